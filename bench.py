@@ -1,0 +1,474 @@
+#!/usr/bin/env python
+"""Benchmark of the routed MoE FFN layer on GB300.
+
+Headline workload: one MoE layer over a 16,384-token prefill chunk (384
+experts, top-8, H=4096, I=2048, bf16, Zipf(1.1)-skewed router logits, fat
+threshold 32).  A step is one moe_forward: route, route lists, both expert
+paths and the combine.  Decode batches 1 and 4 on the same layer are
+reported beside it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Prints one JSON line.  --impl reference times the CPU oracle on a bounded
+token sample of the same workload on the host cores.  Under torchrun
+(N > 1) every rank runs its own replica of the layer (no data exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "routed MoE-layer tokens/s (16k prefill chunk; decode batch 1-24) + % roofline"
+PREFILL = synth.PREFILL
+FAT_THRESHOLD = 32
+L2_BYTES = 129 * 2 ** 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=p["hbm_gbs"], bf16_tflops=p["bf16_tflops"],
+                    bf16_tflops_sustained=p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                    source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                    source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- workload
+
+def stage_work(shape, counts_np):
+    """Algorithmic flops and bytes per stage for one step (used for rooflines).
+    Fat experts: counts >= threshold; thin: 0 < counts < threshold."""
+    T, E, k, H, I = shape.T, shape.E, shape.k, shape.H, shape.I
+    P = T * k
+    thr = shape.fat_threshold
+    fat = counts_np >= max(thr, 1)
+    thin = (counts_np > 0) & (counts_np < thr)
+    fat_rows = int(counts_np[fat].sum())
+    thin_rows = int(counts_np[thin].sum())
+    n_fat, n_thin = int(fat.sum()), int(thin.sum())
+    w_gu = 2 * I * H * 2      # gate + up bytes per expert
+    w_d = H * I * 2
+    return {
+        "route": dict(bytes=T * E * 4 + P * 8, flops=0),
+        "permute": dict(bytes=P * 4 * 4 + E * 8, flops=0),
+        "gather": dict(bytes=fat_rows * H * 2 * 2, flops=0),
+        "gemm_gate_up": dict(flops=2 * fat_rows * H * 2 * I,
+                             bytes=n_fat * w_gu + fat_rows * (H + I) * 2),
+        "thin_gate_up": dict(bytes=n_thin * w_gu + thin_rows * (H + I) * 2,
+                             flops=2 * thin_rows * H * 2 * I),
+        "gemm_down": dict(flops=2 * fat_rows * I * H,
+                          bytes=n_fat * w_d + fat_rows * (H + I) * 2),
+        "thin_down": dict(bytes=n_thin * w_d + thin_rows * (H + I) * 2,
+                          flops=2 * thin_rows * I * H),
+        "combine": dict(bytes=P * H * 2 + T * H * 2 + P * 8, flops=0),
+        "_info": dict(fat_experts=n_fat, thin_experts=n_thin, fat_rows=fat_rows,
+                      thin_rows=thin_rows, touched=int((counts_np > 0).sum())),
+    }
+
+
+def roofline_for(stage, work, ms, peaks):
+    w = work[stage]
+    if stage.startswith("gemm"):
+        ach = w["flops"] / (ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        return {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4),
+                "peak_note": f"bf16 dense, sustained, {peaks['source']}"}
+    ach = w["bytes"] / (ms * 1e-3) / 1e9
+    peak = peaks["hbm_gbs"]
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(ach / peak, 4), "peak_note": f"HBM copy, {peaks['source']}"}
+
+
+class Layer:
+    def __init__(self, moe, shape, device, n_logit_sets=1, zipf=synth.ZIPF_S, weights=None):
+        self.moe = moe
+        self.shape = shape
+        self.device = device
+        if weights is None:
+            weights = synth.make_weights(shape.E, shape.H, shape.I, seed=0, layer=0,
+                                         device=device)
+        self.Wg, self.Wu, self.Wd = weights
+        self.x_cpu = synth.make_x(shape.T, shape.H, seed=0)
+        self.logits_cpu = [synth.make_logits(shape.T, shape.E, seed=0, rep=r, zipf_s=zipf)
+                           for r in range(n_logit_sets)]
+        self.x = self.x_cpu.to(device)
+        self.logits = [l.to(device) for l in self.logits_cpu]
+        self.out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=device)
+        self.idx = torch.empty((shape.T, shape.k), dtype=torch.int32, device=device)
+        self.gates = torch.empty((shape.T, shape.k), dtype=torch.float32, device=device)
+        self.ws = moe.Workspace(moe.workspace_size(shape), device)
+
+    def forward(self, i=0, events=None, logits=None, x=None, out=None):
+        lg = logits if logits is not None else self.logits[i % len(self.logits)]
+        args = (self.shape, lg, x if x is not None else self.x, self.Wg, self.Wu, self.Wd)
+        kw = dict(out=out if out is not None else self.out, topk_idx=self.idx,
+                  gates=self.gates, ws=self.ws)
+        if events is not None:
+            return self.moe.moe_forward_profiled(*args, events, **kw)
+        return self.moe.moe_forward(*args, **kw)
+
+    def counts(self, i=0):
+        self.forward(i)
+        c, _, _, _ = self.moe.moe_permute(self.idx, self.shape.E)
+        torch.cuda.synchronize()
+        return c.cpu().numpy()
+
+
+def time_steps(layer, steps, warmup, profiled=True, rotate=True):
+    moe = layer.moe
+    for i in range(warmup):
+        layer.forward(i)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.PROFILE_EVENTS)]
+          for _ in range(steps)] if profiled else None
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier()
+    start.record()
+    for i in range(steps):
+        layer.forward(i if rotate else 0, events=ev[i] if profiled else None)
+    end.record()
+    torch.cuda.synchronize()
+    barrier()
+    total_ms = start.elapsed_time(end)
+    stage_ms = None
+    if profiled:
+        stage_ms = {}
+        for j, name in enumerate(moe.PROFILE_STAGES):
+            stage_ms[name] = statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev)
+    return total_ms, stage_ms
+
+
+# -------------------------------------------------------- distributed glue
+
+_DIST = {"on": False}
+
+
+def init_dist():
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        _DIST["on"] = True
+        return dist.get_rank(), dist.get_world_size(), int(os.environ.get("LOCAL_RANK", "0"))
+    return 0, 1, 0
+
+
+def barrier():
+    if _DIST["on"]:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float) -> float:
+    if not _DIST["on"]:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------- CPU oracle legs
+
+def oracle_sample(n_tokens, expert_source, logits_np, x_bits, k, seed=123):
+    """Times the oracle on n_tokens sampled tokens of the workload.
+    expert_source(e) -> bf16 bit arrays of expert e (fetched before timing)."""
+    import oracle
+    oracle.build()
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(logits_np.shape[0], size=n_tokens, replace=False))
+    idx, _ = oracle.route(logits_np[toks], k)
+    need = sorted(set(idx.reshape(-1).tolist()))
+    weights = {e: expert_source(e) for e in need}
+    t0 = time.perf_counter()
+    oracle.moe_tokens(x_bits[toks], logits_np[toks], k, weights.__getitem__)
+    dt = time.perf_counter() - t0
+    return n_tokens / dt, dt, len(need)
+
+
+def run_reference(args):
+    """--impl reference: the oracle as it stands, on the host cores, each step
+    a bounded token sample of the prefill workload."""
+    rank, world, _ = init_dist()
+    if rank != 0:
+        return
+    shape = PREFILL
+    x_bits = synth.bf16_bits(synth.make_x(shape.T, shape.H, seed=0))
+    logits_np = synth.make_logits(shape.T, shape.E, seed=0, zipf_s=synth.ZIPF_S).numpy()
+    tokens_per_step = 2
+    cache = {}
+
+    def expert(e):
+        if e not in cache:
+            cache[e] = tuple(synth.bf16_bits(w) for w in synth.make_expert(e, shape.H, shape.I))
+        return cache[e]
+
+    times = []
+    for i in range(args.warmup + args.steps):
+        tps, dt, _ = oracle_sample(tokens_per_step, expert, logits_np, x_bits, shape.k, seed=i)
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = tokens_per_step * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "prefill chunk: T=16384, E=384, top-8, H=4096, I=2048, "
+                               "Zipf(1.1) router bias (oracle on a token sample)",
+                   "tokens_per_step": tokens_per_step},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": 1,
+                         "kind": "oracle",
+                         "sample": f"{tokens_per_step} tokens per step of the 16,384-token "
+                                   "chunk, all of their 8 experts each, single-threaded fp64"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------- GPU bench
+
+def run_gpu(args):
+    rank, world, local = init_dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import routed_expert_ffn_02_gb300 as moe
+    peaks = load_peaks()
+
+    shape = moe.Shape(PREFILL.T, PREFILL.E, PREFILL.k, PREFILL.H, PREFILL.I, FAT_THRESHOLD)
+    layer = Layer(moe, shape, dev, n_logit_sets=1)
+    counts = layer.counts()
+    work = stage_work(shape, counts)
+
+    with ClockSampler(local) as clk:
+        total_ms, stage_ms = time_steps(layer, args.steps, args.warmup)
+    total_ms = max_over_ranks(total_ms)
+    ms_per_step = total_ms / args.steps
+    value = world * shape.T * args.steps / (total_ms * 1e-3)
+
+    dominant = max(stage_ms, key=stage_ms.get)
+    roof = roofline_for(dominant, work, stage_ms[dominant], peaks)
+    roof["kernel"] = dominant
+    roof["traffic"] = args.traffic
+    stages = {s: {"ms": round(stage_ms[s], 4), **{k2: v2 for k2, v2 in
+                                                 roofline_for(s, work, max(stage_ms[s], 1e-6),
+                                                              peaks).items()
+                                                 if k2 in ("achieved", "unit", "frac")}}
+              for s in stage_ms}
+    layer_ideal_ms = max(
+        (work["gemm_gate_up"]["flops"] + work["gemm_down"]["flops"]
+         + work["thin_gate_up"]["flops"] + work["thin_down"]["flops"])
+        / (peaks["bf16_tflops_sustained"] * 1e12),
+        sum(w["bytes"] for n, w in work.items() if not n.startswith("_"))
+        / (peaks["hbm_gbs"] * 1e9)) * 1e3
+
+    # end to end through the C ABI with host buffers: inputs from pinned host
+    # memory, the layer, the output back to pinned host memory, every step.
+    e2e = None
+    if not args.no_e2e:
+        x_h = layer.x_cpu.pin_memory()
+        lg_h = layer.logits_cpu[0].pin_memory()
+        out_h = torch.empty((shape.T, shape.H), dtype=torch.bfloat16).pin_memory()
+        x_d = torch.empty_like(layer.x)
+        lg_d = torch.empty_like(layer.logits[0])
+        out_d = torch.empty_like(layer.out)
+
+        def e2e_step():
+            x_d.copy_(x_h, non_blocking=True)
+            lg_d.copy_(lg_h, non_blocking=True)
+            layer.forward(logits=lg_d, x=x_d, out=out_d)
+            out_h.copy_(out_d, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        barrier()
+        s0.record()
+        for _ in range(args.steps):
+            e2e_step()
+        s1.record()
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = max_over_ranks(s0.elapsed_time(s1))
+        e2e = {"value": round(world * shape.T * args.steps / (e2e_ms * 1e-3), 1),
+               "unit": "tokens/s",
+               "h2d_bytes_per_step": x_h.numel() * 2 + lg_h.numel() * 4,
+               "d2h_bytes_per_step": out_h.numel() * 2,
+               "ms_per_step": round(e2e_ms / args.steps, 4)}
+
+    # decode batches on the same resident layer (secondary lines)
+    decode = {}
+    if not args.no_decode:
+        for B in (1, 4):
+            dshape = moe.Shape(B, PREFILL.E, PREFILL.k, PREFILL.H, PREFILL.I, FAT_THRESHOLD)
+            dl = Layer(moe, dshape, dev, n_logit_sets=8, weights=(layer.Wg, layer.Wu, layer.Wd))
+            dcounts = dl.counts()
+            dwork = stage_work(dshape, dcounts)
+            reps = max(args.steps, 50)
+            dt, dst = time_steps(dl, reps, max(args.warmup, 5))
+            dt = max_over_ranks(dt)
+            bytes_step = sum(w["bytes"] for n, w in dwork.items() if not n.startswith("_"))
+            decode[f"B{B}"] = {
+                "tokens_per_s": round(world * B * reps / (dt * 1e-3), 1),
+                "us_per_step": round(1e3 * dt / reps, 2),
+                "touched_experts": dwork["_info"]["touched"],
+                "weight_stream_frac_of_hbm": round(
+                    (dwork["thin_gate_up"]["bytes"] + dwork["thin_down"]["bytes"])
+                    / ((dst["thin_gate_up"] + dst["thin_down"]) * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                "layer_frac_of_hbm_roofline": round(
+                    bytes_step / (dt / reps * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                "stage_us": {s: round(1e3 * v, 2) for s, v in dst.items()},
+            }
+            del dl
+
+    # CPU baseline: the oracle on a bounded token sample of this workload
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        def expert(e):
+            return tuple(synth.bf16_bits(w[e]) for w in (layer.Wg, layer.Wu, layer.Wd))
+        n = args.cpu_tokens
+        tps, dt, n_exp = oracle_sample(n, expert, layer.logits_cpu[0].numpy(),
+                                       synth.bf16_bits(layer.x_cpu), shape.k)
+        cpu = {"value": round(tps, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} tokens of the 16,384-token chunk with all their experts "
+                         f"({n * shape.k} token-expert pairs, {n_exp} experts), "
+                         f"single-threaded fp64, {dt:.1f} s"}
+
+    launches = moe.forward_launches(shape) * args.steps
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {
+                "workload": "prefill chunk: 1 MoE layer, T=16384 tokens, E=384 experts, top-8, "
+                            "H=4096, I=2048, bf16, Zipf(1.1) router bias, fat threshold 32",
+                "parallelism": "replicas only" if world > 1 else "single GPU",
+                "l2": "inputs larger than L2 (19.3 GB of expert weights per layer)",
+                "fat_experts": work["_info"]["fat_experts"],
+                "thin_experts": work["_info"]["thin_experts"],
+                "touched_experts": work["_info"]["touched"],
+            },
+            "roofline": roof,
+            "layer_roofline": {"ideal_ms": round(layer_ideal_ms, 4),
+                               "frac": round(layer_ideal_ms / ms_per_step, 4),
+                               "note": "max(all flops / bf16 sustained peak, all algorithmic "
+                                       "bytes / HBM peak) over the whole layer"},
+            "stages": stages,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+            "decode": decode,
+            "peaks": peaks,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=48)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the dominant kernel from an ncu capture")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,212 @@
+/*
+ * moe.h -- C ABI of libmoe, the routed mixture-of-experts FFN layer on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The layer (dsv41-flash-offload wiki, overview: "384 routed experts" per MoE
+ * layer, busy experts run as dense GEMMs; file map: route lists with positive
+ * counts, split/combine on the GPU) computes, for T tokens, E experts,
+ * top-k routing, hidden size H and expert intermediate size I:
+ *
+ *   route    : per token, the k largest router logits (ties to the lower
+ *              expert index; outputs in that order) and gates
+ *              g_j = exp(l_j - l_max) / sum_i exp(l_i - l_max) over the k
+ *              selected logits;
+ *   permute  : per-expert counts, their exclusive prefix sum (offsets) and a
+ *              stable counting sort of the T*k token slots (slot s = t*k + j)
+ *              by expert; within an expert, slots ascend;
+ *   expert   : per slot routed to expert e, SwiGLU
+ *              y = W_down[e] . (silu(W_gate[e] . x) * (W_up[e] . x));
+ *              experts holding >= fat_threshold slots (default 32, the
+ *              "fat threshold" of the model page's launch flags) run on the
+ *              tensor-core grouped GEMM, the rest on the weight-streaming path;
+ *   combine  : out_t = sum_j g_j * y_{t,j}, fp32 in fixed j order, rounded to
+ *              bf16.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers unless stated otherwise; the caller owns
+ *     every buffer.  Nothing here allocates device memory; scratch lives in
+ *     the caller's workspace ("ws").  Buffers must be 16-byte aligned, the
+ *     workspace 256-byte aligned.
+ *   - bf16 tensors are passed as moe_bf16 (the raw 16-bit pattern).
+ *   - Layouts are row-major:  logits fp32 [T, E]; x bf16 [T, H];
+ *     W_gate, W_up bf16 [E, I, H]; W_down bf16 [E, H, I] (the [out, in]
+ *     convention, contiguous along the reduction dimension); topk_idx int32
+ *     [T, k]; gates fp32 [T, k]; counts int32 [E]; offsets int32 [E + 1];
+ *     perm, inv_perm int32 [T*k]; y_sorted bf16 [T*k, H]; out bf16 [T, H].
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  The return value covers argument validation and the
+ *     kernel launches; it is MOE_OK or an error code, and moe_last_error()
+ *     gives a message for the calling thread.  Faults inside kernels surface
+ *     from later CUDA calls.  Kernels never trap: a condition found on the
+ *     device (a routed index outside [0, E), a bounded wait that ran out)
+ *     is recorded in the workspace's status word, read with
+ *     moe_workspace_status().
+ *   - Limits: 1 <= k <= min(E, 8); 1 <= E <= 1024; T >= 0 with T*k < 2^31;
+ *     H and I positive multiples of 256; 0 <= fat_threshold <= 33 (experts
+ *     with fewer slots than the threshold take the weight-streaming path,
+ *     which holds at most 32 slots per expert).
+ *   - Preconditions not checked: logits hold no NaN and no +inf, and each
+ *     token's largest logit is finite; buffers do not overlap unless stated.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;            /* bf16 bit pattern */
+typedef struct CUstream_st* moe_stream_t;  /* same type as cudaStream_t */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* bad size, null or misaligned pointer */
+    MOE_ERR_UNSUPPORTED = 2,   /* no sm_103a device, or outside the limits */
+    MOE_ERR_WORKSPACE = 3,     /* ws too small or misaligned */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+    MOE_ERR_TIMEOUT = 5,       /* device status: a bounded wait ran out */
+    MOE_ERR_BAD_INDEX = 6      /* device status: routed index outside [0, E) */
+} moe_status;
+
+typedef struct {
+    int32_t T;              /* tokens */
+    int32_t E;              /* routed experts */
+    int32_t k;              /* experts per token */
+    int32_t H;              /* hidden size */
+    int32_t I;              /* expert intermediate size */
+    int32_t fat_threshold;  /* slots at which an expert takes the GEMM; 32 */
+} moe_shape;
+
+/* ---- routing -------------------------------------------------------- */
+
+/* Top-k router (dsv41-flash-offload wiki, overview: each token is routed to
+ * k of the layer's experts).  Selection compares the raw fp32 logits with
+ * (value descending, index ascending); gates are the softmax over the k
+ * selected logits, computed in fp32.
+ *   logits   [T, E] fp32, read only.
+ *   topk_idx [T, k] int32, written; gates [T, k] fp32, written.
+ * Errors: MOE_ERR_INVALID_ARG for bad sizes or null pointers (T == 0 is a
+ * no-op). */
+moe_status moe_route(const float* logits, int32_t T, int32_t E, int32_t k,
+                     int32_t* topk_idx, float* gates, moe_stream_t stream);
+
+/* ---- route lists ----------------------------------------------------- */
+
+/* Bytes of workspace moe_permute needs for these sizes. */
+size_t moe_permute_workspace_size(int32_t T, int32_t E, int32_t k);
+
+/* Per-expert route lists (dsv41-flash-offload wiki, file map: route lists
+ * with positive counts): counts[e] = #slots routed to e; offsets = exclusive
+ * prefix sum with offsets[E] = T*k; perm[p] = slot at sorted position p
+ * (expert-major, slots ascending within an expert); inv_perm[s] = position of
+ * slot s.  Bit-exact: the result is unique.
+ *   topk_idx [T, k] int32, read only; counts, offsets, perm, inv_perm
+ *   written.  ws: scratch of moe_permute_workspace_size() bytes, whose status
+ *   word must have been cleared once with moe_workspace_init().
+ * A routed index outside [0, E) is skipped and sets MOE_ERR_BAD_INDEX in the
+ * workspace status; the outputs are then unspecified. */
+moe_status moe_permute(const int32_t* topk_idx, int32_t T, int32_t E, int32_t k,
+                       int32_t* counts, int32_t* offsets, int32_t* perm,
+                       int32_t* inv_perm, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
+
+/* ---- experts ----------------------------------------------------------- */
+
+/* Bytes of workspace moe_expert_ffn needs for this shape. */
+size_t moe_expert_ffn_workspace_size(const moe_shape* shape);
+
+/* Expert SwiGLU FFN over the sorted slots (dsv41-flash-offload wiki,
+ * overview: busy experts run as dense GEMMs; model page launch flags: fat
+ * threshold 32).  For sorted position p with slot s = perm[p], token
+ * t = s / k and expert e (offsets[e] <= p < offsets[e+1]):
+ *   y_sorted[p] = bf16( W_down[e] . bf16( silu(W_gate[e] . x[t]) * (W_up[e] . x[t]) ) )
+ * with fp32 accumulation; the intermediate is rounded to bf16 once.
+ * Experts with counts[e] >= fat_threshold run on the tcgen05 grouped GEMM,
+ * experts with 0 < counts[e] < fat_threshold on the weight-streaming path.
+ *   x [T, H], W_gate/W_up [E, I, H], W_down [E, H, I] bf16, read only;
+ *   perm, offsets, counts as moe_permute wrote them; y_sorted [T*k, H] bf16
+ *   written.  ws: moe_expert_ffn_workspace_size() bytes, initialised once
+ *   with moe_workspace_init(). */
+moe_status moe_expert_ffn(const moe_shape* shape, const moe_bf16* x,
+                          const int32_t* perm, const int32_t* offsets,
+                          const int32_t* counts, const moe_bf16* W_gate,
+                          const moe_bf16* W_up, const moe_bf16* W_down,
+                          moe_bf16* y_sorted, void* ws, size_t ws_bytes,
+                          moe_stream_t stream);
+
+/* ---- combine --------------------------------------------------------- */
+
+/* Gate-weighted un-permute (dsv41-flash-offload wiki, file map:
+ * split/combine on the GPU):
+ *   out[t] = bf16( sum_{j=0}^{k-1} gates[t, j] * y_sorted[inv_perm[t*k + j]] )
+ * accumulated in fp32 in ascending j, no atomics: run-to-run identical.
+ *   y_sorted [T*k, H] bf16, inv_perm [T*k], gates [T, k] read only;
+ *   out [T, H] bf16 written (must not overlap y_sorted). */
+moe_status moe_combine(const moe_bf16* y_sorted, const int32_t* inv_perm,
+                       const float* gates, int32_t T, int32_t k, int32_t H,
+                       moe_bf16* out, moe_stream_t stream);
+
+/* ---- whole layer ----------------------------------------------------- */
+
+/* Bytes of workspace moe_forward needs for this shape. */
+size_t moe_workspace_size(const moe_shape* shape);
+
+/* route -> permute -> expert -> combine on one stream, no host
+ * synchronisation.  logits [T, E] fp32, x [T, H] bf16, weights as above;
+ * out [T, H] bf16 written.  topk_idx [T, k] / gates [T, k] may be NULL; when
+ * given they receive the routing.  ws: moe_workspace_size() bytes,
+ * initialised once with moe_workspace_init(). */
+moe_status moe_forward(const moe_shape* shape, const float* logits,
+                       const moe_bf16* x, const moe_bf16* W_gate,
+                       const moe_bf16* W_up, const moe_bf16* W_down,
+                       moe_bf16* out, int32_t* topk_idx, float* gates,
+                       void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Number of stage events moe_forward_profiled records. */
+#define MOE_PROFILE_EVENTS 9
+
+/* moe_forward, recording caller-created CUDA events (cudaEvent_t, passed as
+ * void*) on `stream` at the stage boundaries, so a caller can time each
+ * kernel on the stream it runs on:
+ *   [0] before routing       [1] after routing        [2] after route lists
+ *   [3] after the GEMM row gather                     [4] after the gate/up GEMM
+ *   [5] after the thin gate/up                        [6] after the down GEMM
+ *   [7] after the thin down  [8] after the combine
+ * A stage with nothing to do still records its event.  stage_events must
+ * hold n_events >= MOE_PROFILE_EVENTS entries; a NULL entry is skipped.
+ * Results are identical to moe_forward. */
+moe_status moe_forward_profiled(const moe_shape* shape, const float* logits,
+                                const moe_bf16* x, const moe_bf16* W_gate,
+                                const moe_bf16* W_up, const moe_bf16* W_down,
+                                moe_bf16* out, int32_t* topk_idx, float* gates,
+                                void* ws, size_t ws_bytes, moe_stream_t stream,
+                                void* const* stage_events, int32_t n_events);
+
+/* Number of kernels one moe_forward call with this shape launches (the
+ * launch sequence depends only on the shape), or -1 for an invalid shape. */
+int32_t moe_forward_launches(const moe_shape* shape);
+
+/* ---- workspace status ---------------------------------------------- */
+
+/* Clears the status word of a fresh workspace (asynchronous on stream). */
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Synchronises `stream`, then returns the workspace's device status:
+ * MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_BAD_INDEX (MOE_ERR_CUDA if the copy
+ * fails).  The status is sticky; clear != 0 resets it to MOE_OK. */
+moe_status moe_workspace_status(void* ws, moe_stream_t stream, int32_t clear);
+
+/* Message for the last error returned to the calling thread ("" if none). */
+const char* moe_last_error(void);
+
+/* Library version string. */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

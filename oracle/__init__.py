@@ -60,6 +60,8 @@ def _load():
             lib.oracle_moe_tokens.argtypes = [i64, P, P, i32, i32, i32, i32,
                                               P, P, P, P, P, P]
             lib.oracle_moe_tokens.restype = i32
+            lib.oracle_combine.argtypes = [P, P, P, i64, i32, i32, P]
+            lib.oracle_combine.restype = i32
             lib.oracle_array_to_bf16.argtypes = [P, i64, P]
             lib.oracle_array_to_bf16.restype = None
             lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
@@ -176,3 +178,17 @@ def moe_tokens(x_bits: np.ndarray, logits: np.ndarray, k: int, expert_weights):
     if rc != 0:
         raise OracleError(f"oracle_moe_tokens failed ({rc})")
     return out, oidx, ogates
+
+
+def combine(y_sorted: np.ndarray, inv_perm: np.ndarray, gates: np.ndarray):
+    """out[t] = sum_j gates[t, j] * y_sorted[inv_perm[t*k + j]] in fp64.
+    y_sorted: float [T*k, H]; inv_perm: int [T*k]; gates: float [T, k]."""
+    y = _c(y_sorted, np.float64)
+    ip = _c(inv_perm, np.int32).reshape(-1)
+    g = _c(gates, np.float64)
+    T, k = g.shape
+    H = y.shape[1]
+    out = np.empty((T, H), dtype=np.float64)
+    if _load().oracle_combine(_ptr(y), _ptr(ip), _ptr(g), T, k, H, _ptr(out)) != 0:
+        raise OracleError("inv_perm out of range")
+    return out

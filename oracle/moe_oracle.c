@@ -282,3 +282,30 @@ done:
     free(y);
     return rc;
 }
+
+/* ------------------------------------------------------------------ */
+/* 4. Combine on its own                                               */
+/* ------------------------------------------------------------------ */
+
+/* out[t] = sum_j gates[t*k+j] * y_sorted[inv_perm[t*k+j]], fp64, j ascending.
+ *   y_sorted: fp64 [T*k, H]; inv_perm: int32 [T*k]; gates: fp64 [T*k];
+ *   out: fp64 [T, H]. */
+int oracle_combine(const double* y_sorted, const int32_t* inv_perm, const double* gates,
+                   int64_t T, int k, int H, double* out)
+{
+    int64_t P = T * (int64_t)k;
+    for (int64_t t = 0; t < T; ++t) {
+        double* o = out + t * (int64_t)H;
+        for (int c = 0; c < H; ++c)
+            o[c] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int64_t p = inv_perm[t * k + j];
+            if (p < 0 || p >= P)
+                return -1;
+            const double* y = y_sorted + p * (int64_t)H;
+            for (int c = 0; c < H; ++c)
+                o[c] += gates[t * k + j] * y[c];
+        }
+    }
+    return 0;
+}

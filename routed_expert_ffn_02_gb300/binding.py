@@ -1,0 +1,254 @@
+"""Thin ctypes binding of libmoe (include/moe.h).
+
+Argument marshalling only: every step of the layer runs in libmoe's CUDA
+kernels.  Tensors are torch CUDA tensors; their data pointers and the current
+torch stream are handed to the C entry points.  Missing outputs and
+workspaces are allocated with torch (device memory is torch's job here).  If
+libmoe.so is missing this module raises on import: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with "
+        "`python -c 'import __graft_entry__ as g; g.build()'` "
+        "or `python routed_expert_ffn_02_gb300/_build.py`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+                3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT",
+                6: "MOE_ERR_BAD_INDEX"}
+
+# Every function declared in include/moe.h.
+EXPORTED = ("moe_route", "moe_permute_workspace_size", "moe_permute",
+            "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
+            "moe_workspace_size", "moe_forward", "moe_forward_profiled",
+            "moe_forward_launches", "moe_workspace_init",
+            "moe_workspace_status", "moe_last_error", "moe_version")
+
+
+class MoeShape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("H", ctypes.c_int32), ("I", ctypes.c_int32),
+                ("fat_threshold", ctypes.c_int32)]
+
+
+@dataclass(frozen=True)
+class Shape:
+    T: int
+    E: int
+    k: int
+    H: int
+    I: int
+    fat_threshold: int = 32
+
+    def c(self) -> MoeShape:
+        return MoeShape(self.T, self.E, self.k, self.H, self.I, self.fat_threshold)
+
+    @property
+    def P(self) -> int:
+        return self.T * self.k
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = _lib.moe_last_error().decode()
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+_P = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_sz = ctypes.c_size_t
+_SP = ctypes.POINTER(MoeShape)
+
+_sig = {
+    "moe_route": ([_P, _i32, _i32, _i32, _P, _P, _P], _i32),
+    "moe_permute_workspace_size": ([_i32, _i32, _i32], _sz),
+    "moe_permute": ([_P, _i32, _i32, _i32, _P, _P, _P, _P, _P, _sz, _P], _i32),
+    "moe_expert_ffn_workspace_size": ([_SP], _sz),
+    "moe_expert_ffn": ([_SP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _sz, _P], _i32),
+    "moe_combine": ([_P, _P, _P, _i32, _i32, _i32, _P, _P], _i32),
+    "moe_workspace_size": ([_SP], _sz),
+    "moe_forward": ([_SP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _sz, _P], _i32),
+    "moe_forward_profiled": ([_SP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _sz, _P,
+                              ctypes.POINTER(ctypes.c_void_p), _i32], _i32),
+    "moe_forward_launches": ([_SP], _i32),
+    "moe_workspace_init": ([_P, _sz, _P], _i32),
+    "moe_workspace_status": ([_P, _P, _i32], _i32),
+    "moe_last_error": ([], ctypes.c_char_p),
+    "moe_version": ([], ctypes.c_char_p),
+}
+for _name, (_args, _ret) in _sig.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = _ret
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    assert t.is_cuda and t.is_contiguous(), "expected a contiguous CUDA tensor"
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def version() -> str:
+    return _lib.moe_version().decode()
+
+
+class Workspace:
+    """Device scratch for libmoe calls: a 256-byte-aligned torch buffer whose
+    status word is cleared once at creation."""
+
+    def __init__(self, nbytes: int, device=None, stream=None):
+        device = device or torch.device("cuda", torch.cuda.current_device())
+        self._buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+        off = (-self._buf.data_ptr()) % 256
+        self.tensor = self._buf[off:off + nbytes]
+        self.nbytes = nbytes
+        _check(_lib.moe_workspace_init(self.ptr, nbytes, _stream(stream)), "moe_workspace_init")
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.tensor.data_ptr())
+
+    def status(self, clear: bool = True, stream=None) -> int:
+        """Synchronises the stream and returns the device status code."""
+        return _lib.moe_workspace_status(self.ptr, _stream(stream), int(clear))
+
+
+def workspace_size(shape: Shape) -> int:
+    n = _lib.moe_workspace_size(ctypes.byref(shape.c()))
+    if n == 0:
+        raise MoeError(1, "moe_workspace_size")
+    return n
+
+
+def permute_workspace_size(T: int, E: int, k: int) -> int:
+    n = _lib.moe_permute_workspace_size(T, E, k)
+    if n == 0:
+        raise MoeError(1, "moe_permute_workspace_size")
+    return n
+
+
+def expert_ffn_workspace_size(shape: Shape) -> int:
+    n = _lib.moe_expert_ffn_workspace_size(ctypes.byref(shape.c()))
+    if n == 0:
+        raise MoeError(1, "moe_expert_ffn_workspace_size")
+    return n
+
+
+def moe_route(logits: torch.Tensor, k: int, topk_idx=None, gates=None, stream=None):
+    T, E = logits.shape
+    dev = logits.device
+    topk_idx = topk_idx if topk_idx is not None else torch.empty((T, k), dtype=torch.int32, device=dev)
+    gates = gates if gates is not None else torch.empty((T, k), dtype=torch.float32, device=dev)
+    _check(_lib.moe_route(_ptr(logits), T, E, k, _ptr(topk_idx), _ptr(gates), _stream(stream)),
+           "moe_route")
+    return topk_idx, gates
+
+
+def moe_permute(topk_idx: torch.Tensor, E: int, ws: Workspace | None = None, out=None,
+                stream=None):
+    """Returns (counts [E], offsets [E+1], perm [T*k], inv_perm [T*k])."""
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    P = T * k
+    if out is None:
+        out = (torch.empty(E, dtype=torch.int32, device=dev),
+               torch.empty(E + 1, dtype=torch.int32, device=dev),
+               torch.empty(max(P, 1), dtype=torch.int32, device=dev)[:P],
+               torch.empty(max(P, 1), dtype=torch.int32, device=dev)[:P])
+    counts, offsets, perm, inv_perm = out
+    ws = ws or Workspace(permute_workspace_size(T, E, k), dev, stream)
+    _check(_lib.moe_permute(_ptr(topk_idx), T, E, k, _ptr(counts), _ptr(offsets), _ptr(perm),
+                            _ptr(inv_perm), ws.ptr, ws.nbytes, _stream(stream)), "moe_permute")
+    return counts, offsets, perm, inv_perm
+
+
+def moe_expert_ffn(shape: Shape, x, perm, offsets, counts, W_gate, W_up, W_down,
+                   y_sorted=None, ws: Workspace | None = None, stream=None):
+    dev = x.device
+    y_sorted = y_sorted if y_sorted is not None else torch.empty(
+        (shape.P, shape.H), dtype=torch.bfloat16, device=dev)
+    ws = ws or Workspace(expert_ffn_workspace_size(shape), dev, stream)
+    _check(_lib.moe_expert_ffn(ctypes.byref(shape.c()), _ptr(x), _ptr(perm), _ptr(offsets),
+                               _ptr(counts), _ptr(W_gate), _ptr(W_up), _ptr(W_down),
+                               _ptr(y_sorted), ws.ptr, ws.nbytes, _stream(stream)),
+           "moe_expert_ffn")
+    return y_sorted
+
+
+def moe_combine(y_sorted, inv_perm, gates, T: int, k: int, H: int, out=None, stream=None):
+    out = out if out is not None else torch.empty((T, H), dtype=torch.bfloat16,
+                                                  device=y_sorted.device)
+    _check(_lib.moe_combine(_ptr(y_sorted), _ptr(inv_perm), _ptr(gates), T, k, H, _ptr(out),
+                            _stream(stream)), "moe_combine")
+    return out
+
+
+def moe_forward(shape: Shape, logits, x, W_gate, W_up, W_down, out=None, topk_idx=None,
+                gates=None, ws: Workspace | None = None, stream=None):
+    dev = x.device
+    out = out if out is not None else torch.empty((shape.T, shape.H), dtype=torch.bfloat16,
+                                                  device=dev)
+    ws = ws or Workspace(workspace_size(shape), dev, stream)
+    _check(_lib.moe_forward(ctypes.byref(shape.c()), _ptr(logits), _ptr(x), _ptr(W_gate),
+                            _ptr(W_up), _ptr(W_down), _ptr(out), _ptr(topk_idx), _ptr(gates),
+                            ws.ptr, ws.nbytes, _stream(stream)), "moe_forward")
+    return out
+
+
+PROFILE_EVENTS = 9
+PROFILE_STAGES = ("route", "permute", "gather", "gemm_gate_up", "thin_gate_up",
+                  "gemm_down", "thin_down", "combine")
+
+
+def moe_forward_profiled(shape: Shape, logits, x, W_gate, W_up, W_down, events, out=None,
+                         topk_idx=None, gates=None, ws: Workspace | None = None,
+                         stream=None):
+    """moe_forward recording `events` (PROFILE_EVENTS torch.cuda.Event objects,
+    created with enable_timing=True) at the stage boundaries."""
+    assert len(events) == PROFILE_EVENTS
+    dev = x.device
+    out = out if out is not None else torch.empty((shape.T, shape.H), dtype=torch.bfloat16,
+                                                  device=dev)
+    ws = ws or Workspace(workspace_size(shape), dev, stream)
+    arr = (ctypes.c_void_p * PROFILE_EVENTS)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(_lib.moe_forward_profiled(ctypes.byref(shape.c()), _ptr(logits), _ptr(x),
+                                     _ptr(W_gate), _ptr(W_up), _ptr(W_down), _ptr(out),
+                                     _ptr(topk_idx), _ptr(gates), ws.ptr, ws.nbytes,
+                                     _stream(stream), arr, PROFILE_EVENTS),
+           "moe_forward_profiled")
+    return out
+
+
+def forward_launches(shape: Shape) -> int:
+    """Kernels one moe_forward call launches for this shape."""
+    return _lib.moe_forward_launches(ctypes.byref(shape.c()))
+
+
+def raw_lib():
+    """The loaded ctypes library (for callers that pass raw pointers)."""
+    return _lib

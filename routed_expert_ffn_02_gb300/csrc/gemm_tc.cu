@@ -1,0 +1,496 @@
+// gemm_tc.cu -- grouped expert GEMMs for "busy" experts on the 5th-generation
+// tensor cores (tcgen05 + TMEM), fed by TMA.
+//
+// Experts holding at least the fat threshold of slots run as dense GEMMs
+// (dsv41-flash-offload wiki, overview: busy experts run as FP16 GEMMs; model
+// page launch flags: fat threshold 32).  Here the GEMMs are bf16 with fp32
+// accumulation, over variable-size groups, scheduled entirely on the device:
+//
+//   gate/up:  h[rows, n0:n0+128] = silu(A Wg_e[n0:n0+128]^T) * (A Wu_e[n0:n0+128]^T)
+//             A = x_sorted[rows, :H]; one MMA of N = 256 covers the gate and
+//             up halves, which TMA places back to back in shared memory, so
+//             SiLU*up is fused into the epilogue.
+//   down:     y[rows, n0:n0+256] = h[rows, :I] Wd_e[n0:n0+256]^T
+//
+// The row tiles (128 slots of one expert) come from the planner in device
+// memory, so there is no host synchronisation.  Each CTA is persistent
+// (one per SM) and warp-specialised:
+//   warp 0      TMA producer (one lane): A and B tiles, 64-wide K blocks,
+//               128-byte swizzle, 4-stage ring guarded by mbarriers;
+//   warp 1      MMA issuer (one lane): tcgen05.mma kind::f16, M=128, N=256,
+//               K=16, fp32 accumulators in TMEM, two accumulator buffers
+//               (2 x 256 columns) so the epilogue of one tile overlaps the
+//               main loop of the next;
+//   warp 2      TMEM allocator;
+//   warps 4-7   epilogue: tcgen05.ld -> activation -> bf16 -> global.
+// Rows of a tile past the expert's end belong to other experts (or are past
+// the tensor and zero-filled by TMA); they are computed and discarded.
+//
+// Every mbarrier wait is bounded; on expiry the kernel records
+// MOE_ERR_TIMEOUT in the workspace status, stops issuing work, waits (bounded)
+// for its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <mutex>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = kTileM;          // 128 rows per tile
+constexpr int BK = 64;              // 64 bf16 = 128 bytes = one swizzle row
+constexpr int BN_MMA = 256;         // MMA N
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KB
+constexpr int B_BYTES = BN_MMA * BK * 2;        // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int TMEM_COLS = 512;                  // two 256-column accumulators
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr long long kWaitCycles = 4000000000LL; // ~2 s at 2 GHz
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
+// N >> 3 at bit 17, M >> 4 at bit 24.
+constexpr uint32_t make_idesc(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+constexpr uint32_t kIdesc = make_idesc(BM, BN_MMA);
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Shared-memory matrix descriptor for a K-major tile written by TMA with
+// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);       // start address
+    d |= (uint64_t)1 << 16;                         // leading byte offset (unused)
+    d |= (uint64_t)(1024 >> 4) << 32;               // stride byte offset
+    d |= (uint64_t)1 << 46;                         // descriptor version
+    d |= (uint64_t)2 << 61;                         // 128-byte swizzle
+    return d;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase with the given parity; false on expiry.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long start = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - start > kWaitCycles) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map,
+                                            uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate));
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+          "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+          "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+          "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+struct GemmArgs {
+    const FatTile* tiles;
+    const WsHeader* hdr_ro;
+    WsHeader* hdr;
+    int n_blocks_n;        // N tiles per expert
+    int k_blocks;          // K / 64
+    int b_rows_per_expert; // rows of the B tensor per expert (I or H)
+    int bn_out;            // output columns per tile (128 gated, 256 down)
+    __nv_bfloat16* out;    // [rows, ld_out]
+    int64_t ld_out;
+};
+
+template <bool kGated>
+__global__ void __launch_bounds__(256, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB0,
+                    const __grid_constant__ CUtensorMap tmB1, GemmArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw);
+    const uint32_t bars = base + STAGES * STAGE_BYTES;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t done_bar = bars + 8u * (2 * STAGES + 4);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 5));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 128);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_map(&tmA);
+        prefetch_map(&tmB0);
+        if (kGated) prefetch_map(&tmB1);
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_holder)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const int n_tiles_m = args.hdr_ro->n_fat_tiles;
+    const int total = n_tiles_m * args.n_blocks_n;
+    const int b_tile_rows = kGated ? 128 : 256;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer ----------------
+        int stage = 0;
+        uint32_t phase = 0;
+        int pending[STAGES];
+        for (int s = 0; s < STAGES; ++s) pending[s] = -1;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            const int mt = t / args.n_blocks_n;
+            const int nt = t % args.n_blocks_n;
+            const FatTile ft = args.tiles[mt];
+            const int brow = ft.expert * args.b_rows_per_expert + nt * b_tile_rows;
+            for (int kb = 0; kb < args.k_blocks; ++kb) {
+                if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sa = base + stage * STAGE_BYTES;
+                const uint32_t sb = sa + A_BYTES;
+                mbar_expect_tx(full_bar(stage), STAGE_BYTES);
+                tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, ft.row0);
+                if (kGated) {
+                    tma_load_2d(sb, &tmB0, full_bar(stage), kb * BK, brow);
+                    tma_load_2d(sb + B_BYTES / 2, &tmB1, full_bar(stage), kb * BK, brow);
+                } else {
+                    tma_load_2d(sb, &tmB0, full_bar(stage), kb * BK, brow);
+                }
+                pending[stage] = (int)phase;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            set_status(args.hdr, MOE_ERR_TIMEOUT);
+            // Let the copies already issued land before the CTA exits.
+            for (int s = 0; s < STAGES; ++s)
+                if (pending[s] >= 0) (void)mbar_wait(full_bar(s), (uint32_t)pending[s]);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        int stage = 0;
+        uint32_t phase = 0;
+        int it = 0;
+        bool ok = true;
+        bool issued = false;
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++it) {
+            const int acc = it & 1;
+            const uint32_t acc_phase = (uint32_t)((it >> 1) & 1);
+            if (*abort_flag || !mbar_wait(tempty_bar(acc), acc_phase ^ 1u)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN_MMA);
+            for (int kb = 0; kb < args.k_blocks; ++kb) {
+                if (*abort_flag || !mbar_wait(full_bar(stage), phase)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = base + stage * STAGE_BYTES;
+                const uint32_t sb = sa + A_BYTES;
+                const uint64_t ad = sw128_desc(sa);
+                const uint64_t bd = sw128_desc(sb);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    // +32 bytes per 16-element K step inside the swizzle row
+                    umma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
+                              (kb > 0 || kk > 0) ? 1u : 0u);
+                }
+                issued = true;
+                umma_commit(empty_bar(stage));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            umma_commit(tfull_bar(acc));
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            set_status(args.hdr, MOE_ERR_TIMEOUT);
+            if (issued) {
+                // Wait for every MMA issued so far before TMEM is freed.
+                umma_commit(done_bar);
+                (void)mbar_wait(done_bar, 0);
+            }
+        }
+    } else if (warp >= 4) {
+        // ---------------- epilogue ----------------
+        const int ew = warp - 4;              // TMEM lanes 32*ew .. 32*ew+31
+        const int row = ew * 32 + lane;
+        int it = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+            const int acc = it & 1;
+            const uint32_t acc_phase = (uint32_t)((it >> 1) & 1);
+            if (*abort_flag || !mbar_wait(tfull_bar(acc), acc_phase)) {
+                *abort_flag = 1;
+                set_status(args.hdr, MOE_ERR_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            const int mt = t / args.n_blocks_n;
+            const int nt = t % args.n_blocks_n;
+            const FatTile ft = args.tiles[mt];
+            const bool valid = row < ft.rows;
+            __nv_bfloat16* dst = args.out + (int64_t)(ft.row0 + row) * args.ld_out +
+                                 (int64_t)nt * args.bn_out;
+            const uint32_t taddr = tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(acc * BN_MMA);
+            if (kGated) {
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 32) {
+                    uint32_t g[32], u[32];
+                    tmem_ld32(taddr + c, g);
+                    tmem_ld32(taddr + 128 + c, u);
+                    tmem_ld_wait();
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const float g0 = __uint_as_float(g[2 * q]), g1 = __uint_as_float(g[2 * q + 1]);
+                        const float u0 = __uint_as_float(u[2 * q]), u1 = __uint_as_float(u[2 * q + 1]);
+                        const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
+                        const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+                        packed[q] = pack_bf16(h0, h1);
+                    }
+                    if (valid) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            d4[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
+                                               packed[4 * q + 3]);
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < 256; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(taddr + c, v);
+                    tmem_ld_wait();
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        packed[q] = pack_bf16(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
+                    if (valid) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            d4[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
+                                               packed[4 * q + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(tempty_bar(acc));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TMEM_COLS));
+    }
+}
+
+// ---- host side -----------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, cols] matrix, box = 64 cols x box_rows,
+// 128-byte swizzle, zero fill outside the tensor.
+cudaError_t make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <bool kGated>
+cudaError_t set_smem_attr() {
+    static cudaError_t err = cudaErrorUnknown;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(grouped_gemm_kernel<kGated>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    });
+    return err;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_alloc,
+                                const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
+                                int E, int H, int I, const Plan& plan,
+                                __nv_bfloat16* h, int num_sms, cudaStream_t s) {
+    CUtensorMap mA, mG, mU;
+    cudaError_t e;
+    if ((e = make_map(&mA, x_sorted, (uint64_t)rows_alloc, (uint64_t)H, BM)) != cudaSuccess) return e;
+    if ((e = make_map(&mG, Wg, (uint64_t)E * I, (uint64_t)H, 128)) != cudaSuccess) return e;
+    if ((e = make_map(&mU, Wu, (uint64_t)E * I, (uint64_t)H, 128)) != cudaSuccess) return e;
+    if ((e = set_smem_attr<true>()) != cudaSuccess) return e;
+    GemmArgs a;
+    a.tiles = plan.tiles;
+    a.hdr_ro = plan.hdr;
+    a.hdr = plan.hdr;
+    a.n_blocks_n = I / 128;
+    a.k_blocks = H / BK;
+    a.b_rows_per_expert = I;
+    a.bn_out = 128;
+    a.out = h;
+    a.ld_out = I;
+    grouped_gemm_kernel<true><<<num_sms, 256, SMEM_BYTES, s>>>(mA, mG, mU, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_down(const __nv_bfloat16* h, int64_t rows_alloc,
+                             const __nv_bfloat16* Wd, int E, int H, int I,
+                             const Plan& plan, __nv_bfloat16* y_sorted,
+                             int num_sms, cudaStream_t s) {
+    CUtensorMap mA, mD;
+    cudaError_t e;
+    if ((e = make_map(&mA, h, (uint64_t)rows_alloc, (uint64_t)I, BM)) != cudaSuccess) return e;
+    if ((e = make_map(&mD, Wd, (uint64_t)E * H, (uint64_t)I, 256)) != cudaSuccess) return e;
+    if ((e = set_smem_attr<false>()) != cudaSuccess) return e;
+    GemmArgs a;
+    a.tiles = plan.tiles;
+    a.hdr_ro = plan.hdr;
+    a.hdr = plan.hdr;
+    a.n_blocks_n = H / 256;
+    a.k_blocks = I / BK;
+    a.b_rows_per_expert = H;
+    a.bn_out = 256;
+    a.out = y_sorted;
+    a.ld_out = H;
+    grouped_gemm_kernel<false><<<num_sms, 256, SMEM_BYTES, s>>>(mA, mD, mD, a);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

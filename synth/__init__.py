@@ -12,7 +12,8 @@ Recipe (the pages print no tensors, so these stand in for the real model's):
     with an optional Zipf-skewed expert bias b_e = -s * ln(rank_e), rank a
     seeded random permutation of 1..E (s = 1.1 for the skewed workloads), so
     expert popularity falls off like rank^-s.
-Seeds: x uses ``seed``, weights ``seed + 1000 + layer``, logits
+Seeds: x uses ``seed``; each expert matrix has its own generator derived
+from (seed, layer, expert, matrix) so single experts can be drawn alone; logits
 ``seed + 2000 + layer + 7919 * rep`` (``rep`` rotates independent logit sets
 so repeated timing runs do not hit the same experts in L2), the Zipf ranks
 ``seed + 3000 + layer``.
@@ -59,22 +60,32 @@ def make_x(T: int, H: int, seed: int = 0, device="cpu") -> torch.Tensor:
                        dtype=torch.float32).to(torch.bfloat16)
 
 
-def _normal_bf16(shape, std: float, g: torch.Generator, device) -> torch.Tensor:
-    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
-    # Fill one leading slice at a time to bound the fp32 staging memory.
-    for e in range(shape[0]):
-        out[e] = (torch.randn(shape[1:], generator=g, device=device,
-                              dtype=torch.float32) * std).to(torch.bfloat16)
-    return out
+def _expert_seed(seed: int, layer: int, e: int, which: int) -> int:
+    # One generator per (layer, expert, matrix), so any single expert can be
+    # drawn on its own.
+    return ((seed + 1000 + layer) * 1_000_003 + e) * 4 + which
+
+
+def make_expert(e: int, H: int, I: int, seed: int = 0, layer: int = 0, device="cpu",
+                std: float = 0.02):
+    """Expert e's (Wg [I, H], Wu [I, H], Wd [H, I]) in bf16."""
+    out = []
+    for which, shp in enumerate(((I, H), (I, H), (H, I))):
+        g = _gen(_expert_seed(seed, layer, e, which), device)
+        out.append((torch.randn(shp, generator=g, device=device, dtype=torch.float32)
+                    * std).to(torch.bfloat16))
+    return tuple(out)
 
 
 def make_weights(E: int, H: int, I: int, seed: int = 0, layer: int = 0,
                  device="cpu", std: float = 0.02):
-    """Returns (Wg [E, I, H], Wu [E, I, H], Wd [E, H, I]) in bf16."""
-    g = _gen(seed + 1000 + layer, device)
-    Wg = _normal_bf16((E, I, H), std, g, device)
-    Wu = _normal_bf16((E, I, H), std, g, device)
-    Wd = _normal_bf16((E, H, I), std, g, device)
+    """Returns (Wg [E, I, H], Wu [E, I, H], Wd [E, H, I]) in bf16; expert e
+    equals make_expert(e, ...) drawn on the same device."""
+    Wg = torch.empty((E, I, H), dtype=torch.bfloat16, device=device)
+    Wu = torch.empty((E, I, H), dtype=torch.bfloat16, device=device)
+    Wd = torch.empty((E, H, I), dtype=torch.bfloat16, device=device)
+    for e in range(E):
+        Wg[e], Wu[e], Wd[e] = make_expert(e, H, I, seed, layer, device, std)
     return Wg, Wu, Wd
 
 

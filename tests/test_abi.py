@@ -1,0 +1,112 @@
+"""C ABI checks that need no GPU: the library loads, exports every function
+include/moe.h declares, and rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from routed_expert_ffn_02_gb300 import _build
+    _build.build()
+    import routed_expert_ffn_02_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s+(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_expected_functions():
+    names = declared_functions()
+    assert "moe_forward" in names and "moe_route" in names and len(names) >= 12
+
+
+def test_library_exports_every_declared_function(moe):
+    lib = moe.binding.raw_lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert sorted(moe.EXPORTED) == declared_functions()
+
+
+def test_version(moe):
+    assert "sm_103a" in moe.version()
+
+
+def test_workspace_sizes(moe):
+    s = moe.Shape(16384, 384, 8, 4096, 2048)
+    n = moe.workspace_size(s)
+    P = s.P
+    # sorted activations (reused for the sorted outputs) and the intermediate dominate
+    assert P * (4096 + 2048) * 2 < n < P * (4096 + 2048) * 2 + 64 * 2 ** 20
+    assert moe.expert_ffn_workspace_size(s) < n
+    assert moe.permute_workspace_size(16384, 384, 8) >= 256
+    small = moe.workspace_size(moe.Shape(1, 384, 8, 4096, 2048))
+    assert small < 4 * 2 ** 20
+
+
+@pytest.mark.parametrize("bad", [
+    dict(T=-1), dict(E=0), dict(E=1025), dict(k=0), dict(k=9), dict(E=4, k=5),
+    dict(H=100), dict(H=0), dict(I=128), dict(fat_threshold=-1), dict(fat_threshold=34),
+])
+def test_bad_shapes_rejected(moe, bad):
+    base = dict(T=16, E=16, k=2, H=512, I=256, fat_threshold=32)
+    base.update(bad)
+    shape = moe.binding.MoeShape(**base)
+    lib = moe.binding.raw_lib()
+    assert lib.moe_workspace_size(ctypes.byref(shape)) == 0
+    st = lib.moe_forward(ctypes.byref(shape), None, None, None, None, None, None, None, None,
+                         None, 0, None)
+    assert st == 1
+    assert lib.moe_last_error()
+
+
+def test_route_argument_errors(moe):
+    lib = moe.binding.raw_lib()
+    assert lib.moe_route(None, 4, 3, 4, None, None, None) == 1       # k > E
+    assert lib.moe_route(None, 4, 3, 2, None, None, None) == 1       # NULL logits
+    assert lib.moe_route(None, 0, 3, 2, None, None, None) == 0       # T == 0: no-op
+    assert lib.moe_permute_workspace_size(4, 3, 9) == 0
+
+
+def test_pointer_and_workspace_errors(moe):
+    lib = moe.binding.raw_lib()
+    shape = moe.binding.MoeShape(16, 16, 2, 512, 256, 32)
+    good = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10008)   # 8-byte aligned only
+    # misaligned activation pointer
+    st = lib.moe_forward(ctypes.byref(shape), good, odd, good, good, good, good, None, None,
+                         good, 1 << 30, None)
+    assert st == 1 and b"aligned" in lib.moe_last_error()
+    # missing / small / misaligned workspace
+    st = lib.moe_forward(ctypes.byref(shape), good, good, good, good, good, good, None, None,
+                         None, 0, None)
+    assert st == 3
+    st = lib.moe_forward(ctypes.byref(shape), good, good, good, good, good, good, None, None,
+                         good, 100, None)
+    assert st == 3
+    st = lib.moe_forward(ctypes.byref(shape), good, good, good, good, good, good, None, None,
+                         ctypes.c_void_p(0x10010), 1 << 30, None)
+    assert st == 3
+    st = lib.moe_permute(good, 16, 16, 2, good, good, good, good, None, 0, None)
+    assert st == 3
+    assert lib.moe_combine(good, good, good, 4, 9, 512, good, None) == 1
+    assert lib.moe_combine(good, good, good, 4, 2, 12, good, None) == 1
+
+
+def test_product_path_does_not_import_oracle():
+    """The library package and its binding never reference the oracle."""
+    pkg = os.path.join(ROOT, "routed_expert_ffn_02_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in src and "from oracle" not in src, f
+                assert "moe_oracle" not in src, f

@@ -1,0 +1,266 @@
+"""GPU parity: expert FFN, combine and the whole layer against the oracle.
+
+Routing indices, counts and the permutation must match bit-exactly; bf16
+outputs within relative RMS 5e-3 and max-abs 2e-2.  Small layers are checked
+on every output; full-size layers on every token whose oracle cost is
+bounded (decode) or on a seeded token sample chosen to cover both expert
+paths (prefill), since each output row depends only on its own token.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import DeviceExperts, GATE_ATOL, assert_close, oracle_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import routed_expert_ffn_02_gb300 as m
+    return m
+
+
+def _to_dev(inp):
+    return {k: v.cuda() for k, v in inp.items()}
+
+
+def _forward(moe, shape, d, profiled=False):
+    T, k = shape.T, shape.k
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gates = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ws = moe.Workspace(moe.workspace_size(shape))
+    if profiled:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(moe.PROFILE_EVENTS)]
+        out = moe.moe_forward_profiled(shape, d["logits"], d["x"], d["Wg"], d["Wu"], d["Wd"],
+                                       ev, topk_idx=idx, gates=gates, ws=ws)
+    else:
+        out = moe.moe_forward(shape, d["logits"], d["x"], d["Wg"], d["Wu"], d["Wd"],
+                              topk_idx=idx, gates=gates, ws=ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    return out, idx, gates
+
+
+def _full_check(moe, s, thr, inp, d=None):
+    d = d or _to_dev(inp)
+    shape = moe.Shape(s.T, s.E, s.k, s.H, s.I, fat_threshold=thr)
+    out, idx, gates = _forward(moe, shape, d)
+    experts = DeviceExperts(d["Wg"], d["Wu"], d["Wd"])
+    ref, ridx, rgates = oracle_rows(synth.bf16_bits(inp["x"]), inp["logits"].numpy(), s.k,
+                                    experts, np.arange(s.T))
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    assert np.allclose(gates.cpu().numpy(), rgates, rtol=0, atol=GATE_ATOL)
+    return assert_close(out, ref, f"forward {s} thr={thr}")
+
+
+# ---------------------------------------------------------------- tiny layer
+
+@pytest.mark.parametrize("thr", [0, 1, 8, 32, 33])
+def test_forward_tiny(moe, thr):
+    """T=64, E=16, top-2, H=512, I=256 (seed 0).  thr=0 sends every expert to
+    the tcgen05 GEMM, thr=32/33 every expert to the weight-streaming path."""
+    inp = synth.make_layer(synth.TINY, seed=0)
+    _full_check(moe, synth.TINY, thr, inp)
+
+
+def test_expert_ffn_and_combine_entry_points(moe):
+    """route -> permute -> expert_ffn -> combine through the separate entry
+    points; y_sorted row by row and out against the oracle."""
+    s = synth.Shape(T=96, E=8, k=3, H=256, I=512)
+    inp = synth.make_layer(s, seed=4, zipf_s=1.1)
+    d = _to_dev(inp)
+    shape = moe.Shape(s.T, s.E, s.k, s.H, s.I, fat_threshold=32)
+    idx, gates = moe.moe_route(d["logits"], s.k)
+    counts, offsets, perm, inv = moe.moe_permute(idx, s.E)
+    y = moe.moe_expert_ffn(shape, d["x"], perm, offsets, counts, d["Wg"], d["Wu"], d["Wd"])
+    out = moe.moe_combine(y, inv, gates, s.T, s.k, s.H)
+    torch.cuda.synchronize()
+    c = counts.cpu().numpy()
+    assert (c >= 32).any() and ((c > 0) & (c < 32)).any(), c   # both paths ran
+    xb = synth.bf16_bits(inp["x"])
+    experts = DeviceExperts(d["Wg"], d["Wu"], d["Wd"])
+    p_perm = perm.cpu().numpy()
+    p_off = offsets.cpu().numpy()
+    y_ref = np.empty((s.P, s.H))
+    for e in range(s.E):
+        for p in range(p_off[e], p_off[e + 1]):
+            _, y_ref[p] = oracle.expert_ffn(xb[p_perm[p] // s.k], *experts(e))
+    assert_close(y, y_ref, "y_sorted")
+    out_ref = oracle.combine(y_ref, inv.cpu().numpy(), gates.cpu().numpy().astype(np.float64))
+    assert_close(out, out_ref, "combine")
+
+
+def test_combine_matches_oracle(moe):
+    T, k, H = 300, 8, 1024
+    g = torch.Generator().manual_seed(9)
+    y = torch.randn((T * k, H), generator=g).to(torch.bfloat16)
+    inv = torch.randperm(T * k, generator=g).to(torch.int32)
+    gates = torch.rand((T, k), generator=g)
+    gates = gates / gates.sum(1, keepdim=True)
+    out = moe.moe_combine(y.cuda(), inv.cuda(), gates.cuda(), T, k, H)
+    torch.cuda.synchronize()
+    ref = oracle.combine(oracle.bf16_bits_to_f64(synth.bf16_bits(y)), inv.numpy(),
+                         gates.numpy().astype(np.float64))
+    assert_close(out, ref, "combine")
+
+
+def _assigned_logits(counts, E):
+    """Logits that send exactly counts[e] tokens to expert e (top-1)."""
+    tok = np.repeat(np.arange(E), counts)
+    rng = np.random.default_rng(0)
+    rng.shuffle(tok)
+    lg = rng.standard_normal((len(tok), E)).astype(np.float32)
+    lg[np.arange(len(tok)), tok] = 10.0
+    return torch.from_numpy(lg)
+
+
+def test_forward_threshold_edges(moe):
+    """Experts with exactly 0, 1, 31, 32, 33, 128, 129 and 255 slots: the
+    fat-threshold boundary and ragged GEMM tiles."""
+    counts = [31, 32, 33, 0, 1, 128, 129, 255]
+    E = len(counts)
+    lg = _assigned_logits(counts, E)
+    s = synth.Shape(T=lg.shape[0], E=E, k=1, H=256, I=256)
+    inp = synth.make_layer(s, seed=6)
+    inp["logits"] = lg
+    rr, _ = _full_check(moe, s, 32, inp)
+    # k = 2 on the same tokens
+    s2 = synth.Shape(T=lg.shape[0], E=E, k=2, H=256, I=256)
+    inp["logits"] = lg
+    _full_check(moe, s2, 32, inp)
+
+
+def test_forward_one_expert_takes_all(moe):
+    s = synth.Shape(T=700, E=4, k=1, H=512, I=256)
+    inp = synth.make_layer(s, seed=7)
+    inp["logits"] = torch.zeros((s.T, s.E))
+    inp["logits"][:, 2] = 1.0
+    _full_check(moe, s, 32, inp)
+
+
+def test_forward_T0_is_noop(moe):
+    shape = moe.Shape(0, 16, 2, 512, 256)
+    x = torch.empty((0, 512), dtype=torch.bfloat16, device="cuda")
+    W = torch.empty((16, 256, 512), dtype=torch.bfloat16, device="cuda")
+    Wd = torch.empty((16, 512, 256), dtype=torch.bfloat16, device="cuda")
+    moe.moe_forward(shape, torch.empty((0, 16), device="cuda"), x, W, W, Wd,
+                    out=torch.empty((1, 512), dtype=torch.bfloat16, device="cuda"))
+
+
+def test_forward_rejects_small_workspace(moe):
+    s = synth.TINY
+    d = _to_dev(synth.make_layer(s, seed=0))
+    shape = moe.Shape(s.T, s.E, s.k, s.H, s.I)
+    ws = moe.Workspace(1024)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_forward(shape, d["logits"], d["x"], d["Wg"], d["Wu"], d["Wd"], ws=ws)
+    assert ei.value.status == 3
+
+
+# ------------------------------------------------------ full-size layer (E=384)
+
+@pytest.fixture(scope="module")
+def big_layer():
+    """One layer of the full model shape, weights generated on the device:
+    384 experts, H=4096, I=2048 (19.3 GB of bf16 weights)."""
+    s = synth.PREFILL
+    Wg, Wu, Wd = synth.make_weights(s.E, s.H, s.I, seed=0, layer=0, device="cuda")
+    yield dict(Wg=Wg, Wu=Wu, Wd=Wd)
+    del Wg, Wu, Wd
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("B", [1, 4])
+def test_forward_decode(moe, big_layer, B):
+    s = synth.Shape(T=B, E=384, k=8, H=4096, I=2048)
+    inp = dict(x=synth.make_x(B, s.H, seed=0), logits=synth.make_logits(B, s.E, seed=0,
+                                                                           zipf_s=synth.ZIPF_S))
+    d = dict(_to_dev(inp), **big_layer)
+    _full_check(moe, s, 32, inp, d)
+
+
+def _sample_tokens(idx_np, counts_np, thr, rng, n_random=24):
+    T = idx_np.shape[0]
+    picks = set(rng.choice(T, size=min(n_random, T), replace=False).tolist())
+    thin = np.where((counts_np > 0) & (counts_np < thr))[0]
+    fat = np.where(counts_np >= thr)[0]
+    thin_tokens = np.where(np.isin(idx_np, thin).any(1))[0]
+    picks.update(rng.choice(thin_tokens, size=min(8, len(thin_tokens)), replace=False).tolist())
+    if len(fat):
+        smallest = fat[np.argmin(counts_np[fat])]
+        hottest = fat[np.argmax(counts_np[fat])]
+        for e in (smallest, hottest):
+            toks = np.where((idx_np == e).any(1))[0]
+            picks.update(toks[:3].tolist())
+    for c in (31, 32, 33):
+        for e in np.where(counts_np == c)[0][:1]:
+            picks.update(np.where((idx_np == e).any(1))[0][:2].tolist())
+    return np.array(sorted(picks))
+
+
+@pytest.mark.parametrize("H,I", [(4096, 2048), (2048, 1024)])
+def test_forward_prefill_sampled(moe, big_layer, H, I):
+    """16,384-token chunk, Zipf(1.1)-skewed routing.  Routing, counts and the
+    permutation are checked on all tokens; outputs on a sample covering random
+    tokens, tokens of thin experts and of the smallest and hottest fat expert."""
+    s = synth.Shape(T=16384, E=384, k=8, H=H, I=I)
+    inp = dict(x=synth.make_x(s.T, H, seed=0),
+               logits=synth.make_logits(s.T, s.E, seed=0, zipf_s=synth.ZIPF_S))
+    if H == 4096:
+        W = big_layer
+    else:
+        Wg, Wu, Wd = synth.make_weights(s.E, H, I, seed=0, layer=0, device="cuda")
+        W = dict(Wg=Wg, Wu=Wu, Wd=Wd)
+    d = dict(_to_dev(inp), **W)
+    shape = moe.Shape(s.T, s.E, s.k, H, I, fat_threshold=32)
+    out, idx, gates = _forward(moe, shape, d)
+    lg = inp["logits"].numpy()
+    ridx, rgates = oracle.route(lg, s.k)
+    idx_np = idx.cpu().numpy()
+    assert np.array_equal(idx_np, ridx)
+    assert np.allclose(gates.cpu().numpy(), rgates, rtol=0, atol=GATE_ATOL)
+    counts, offsets, perm, inv = moe.moe_permute(idx, s.E)
+    rc, ro, rp, ri = oracle.permute(ridx, s.E)
+    assert np.array_equal(counts.cpu().numpy(), rc) and np.array_equal(perm.cpu().numpy(), rp)
+    assert np.array_equal(inv.cpu().numpy(), ri)
+    assert (rc >= 32).sum() > 0 and ((rc > 0) & (rc < 32)).sum() > 0
+    toks = _sample_tokens(ridx, rc, 32, np.random.default_rng(1))
+    experts = DeviceExperts(W["Wg"], W["Wu"], W["Wd"])
+    ref, _, _ = oracle_rows(synth.bf16_bits(inp["x"]), lg, s.k, experts, toks)
+    assert_close(out[torch.from_numpy(toks).cuda()], ref, f"prefill H={H}")
+
+
+def test_forward_deterministic_and_profiled(moe, big_layer):
+    s = synth.Shape(T=2048, E=384, k=8, H=4096, I=2048)
+    inp = dict(x=synth.make_x(s.T, s.H, seed=1),
+               logits=synth.make_logits(s.T, s.E, seed=1, zipf_s=synth.ZIPF_S))
+    d = dict(_to_dev(inp), **big_layer)
+    shape = moe.Shape(s.T, s.E, s.k, s.H, s.I)
+    a, _, _ = _forward(moe, shape, d)
+    b, _, _ = _forward(moe, shape, d)
+    c, _, _ = _forward(moe, shape, d, profiled=True)
+    assert torch.equal(a, b) and torch.equal(a, c)
+
+
+def test_decode_sweep_four_layers(moe):
+    """Decode batch 24 over 4 resident layers (77 GB of weights); two layers
+    checked in full against the oracle, all four for routing."""
+    s = synth.Shape(T=24, E=384, k=8, H=4096, I=2048)
+    layers = [synth.make_weights(s.E, s.H, s.I, seed=0, layer=l, device="cuda")
+              for l in range(4)]
+    x = synth.make_x(s.T, s.H, seed=0)
+    for l, (Wg, Wu, Wd) in enumerate(layers):
+        inp = dict(x=x, logits=synth.make_logits(s.T, s.E, seed=0, layer=l,
+                                                 zipf_s=synth.ZIPF_S))
+        d = dict(_to_dev(inp), Wg=Wg, Wu=Wu, Wd=Wd)
+        if l in (0, 3):
+            _full_check(moe, s, 32, inp, d)
+        else:
+            shape = moe.Shape(s.T, s.E, s.k, s.H, s.I)
+            _, idx, _ = _forward(moe, shape, d)
+            assert np.array_equal(idx.cpu().numpy(), oracle.route(inp["logits"].numpy(), s.k)[0])
+    del layers
+    torch.cuda.empty_cache()

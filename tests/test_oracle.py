@@ -286,3 +286,21 @@ def test_synth_is_deterministic():
         assert torch.equal(a[key], b[key])
     c = synth.make_logits(8, 16, seed=0, rep=1)
     assert not torch.equal(c, synth.make_logits(8, 16, seed=0, rep=0))
+
+
+def test_combine_one_hot_gates_select_rows():
+    # With one-hot gates the combine returns the selected sorted rows exactly.
+    rng = np.random.default_rng(3)
+    T, k, H = 6, 3, 5
+    y = rng.standard_normal((T * k, H))
+    inv = rng.permutation(T * k).astype(np.int32)
+    g = np.zeros((T, k))
+    pick = rng.integers(0, k, T)
+    g[np.arange(T), pick] = 1.0
+    out = oracle.combine(y, inv, g)
+    assert np.array_equal(out, y[inv.reshape(T, k)[np.arange(T), pick]])
+    # and it is linear in the gates
+    g2 = rng.random((T, k))
+    a = oracle.combine(y, inv, g2)
+    b = oracle.combine(y, inv, 2.0 * g2)
+    assert np.allclose(b, 2.0 * a, rtol=1e-15, atol=0)
