@@ -12,8 +12,8 @@ HEADER = os.path.join(ROOT, "include", "moe.h")
 
 @pytest.fixture(scope="module")
 def moe():
-    from routed_expert_ffn_02_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import routed_expert_ffn_02_gb300 as m
     return m
 
