@@ -235,6 +235,9 @@ def moe_forward_profiled(shape: Shape, logits, x, W_gate, W_up, W_down, events, 
     out = out if out is not None else torch.empty((shape.T, shape.H), dtype=torch.bfloat16,
                                                   device=dev)
     ws = ws or Workspace(workspace_size(shape), dev, stream)
+    for e in events:
+        if e.cuda_event == 0:   # torch creates the CUDA event on first record
+            e.record(stream if stream is not None else torch.cuda.current_stream())
     arr = (ctypes.c_void_p * PROFILE_EVENTS)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check(_lib.moe_forward_profiled(ctypes.byref(shape.c()), _ptr(logits), _ptr(x),
                                      _ptr(W_gate), _ptr(W_up), _ptr(W_down), _ptr(out),
