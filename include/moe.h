@@ -113,6 +113,29 @@ moe_status moe_permute(const int32_t* topk_idx, int32_t T, int32_t E, int32_t k,
                        int32_t* inv_perm, void* ws, size_t ws_bytes,
                        moe_stream_t stream);
 
+/* moe_permute without a workspace, for callers that cannot allocate device
+ * memory: a serving process that has already handed all of HBM to weights
+ * and caches and has no pool left to carve a workspace from, or host code
+ * that must keep cudaMalloc (which may synchronise the device) off its hot
+ * path.  The pages describe nothing like it; it exists for such embedders.
+ * Same arguments, results and bit-exactness as moe_permute, minus ws.
+ * Scratch lives in a fixed array inside the library (about 1 MiB, held by
+ * every GPU that loads libmoe until the process exits), so:
+ *   - T*k may not exceed 262144 (MOE_ERR_UNSUPPORTED otherwise);
+ *   - nothing is allocated: no cudaMalloc/cudaFree, no allocating library
+ *     call; the first call on each device looks the array's device address
+ *     up (cudaGetSymbolAddress, that device current) -- make that first call
+ *     before any stream capture;
+ *   - all calls share the array and it keeps the last call's contents; each
+ *     call clears the status it needs.  Calls that overlap on the GPU (e.g.
+ *     on unordered streams) race and give wrong results.
+ * device_status (device int32, may be NULL) receives this call's device
+ * status: MOE_OK or MOE_ERR_BAD_INDEX. */
+moe_status moe_permute_noalloc(const int32_t* topk_idx, int32_t T, int32_t E, int32_t k,
+                               int32_t* counts, int32_t* offsets, int32_t* perm,
+                               int32_t* inv_perm, int32_t* device_status,
+                               moe_stream_t stream);
+
 /* ---- experts ----------------------------------------------------------- */
 
 /* Bytes of workspace moe_expert_ffn needs for this shape. */

@@ -31,7 +31,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 6: "MOE_ERR_BAD_INDEX"}
 
 # Every function declared in include/moe.h.
-EXPORTED = ("moe_route", "moe_permute_workspace_size", "moe_permute",
+EXPORTED = ("moe_route", "moe_permute_workspace_size", "moe_permute", "moe_permute_noalloc",
             "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
             "moe_workspace_size", "moe_forward", "moe_forward_profiled",
             "moe_forward_launches", "moe_workspace_init",
@@ -77,6 +77,7 @@ _sig = {
     "moe_route": ([_P, _i32, _i32, _i32, _P, _P, _P], _i32),
     "moe_permute_workspace_size": ([_i32, _i32, _i32], _sz),
     "moe_permute": ([_P, _i32, _i32, _i32, _P, _P, _P, _P, _P, _sz, _P], _i32),
+    "moe_permute_noalloc": ([_P, _i32, _i32, _i32, _P, _P, _P, _P, _P, _P], _i32),
     "moe_expert_ffn_workspace_size": ([_SP], _sz),
     "moe_expert_ffn": ([_SP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _sz, _P], _i32),
     "moe_combine": ([_P, _P, _P, _i32, _i32, _i32, _P, _P], _i32),
@@ -185,6 +186,18 @@ def moe_permute(topk_idx: torch.Tensor, E: int, ws: Workspace | None = None, out
     _check(_lib.moe_permute(_ptr(topk_idx), T, E, k, _ptr(counts), _ptr(offsets), _ptr(perm),
                             _ptr(inv_perm), ws.ptr, ws.nbytes, _stream(stream)), "moe_permute")
     return counts, offsets, perm, inv_perm
+
+
+def moe_permute_noalloc(topk_idx: torch.Tensor, E: int, out, device_status=None, stream=None):
+    """moe_permute with the library's fixed scratch (no workspace, no device
+    allocation inside the call).  `out` = (counts, offsets, perm, inv_perm)
+    must be supplied by the caller; device_status (int32 [1]) is optional."""
+    T, k = topk_idx.shape
+    counts, offsets, perm, inv_perm = out
+    _check(_lib.moe_permute_noalloc(_ptr(topk_idx), T, E, k, _ptr(counts), _ptr(offsets),
+                                    _ptr(perm), _ptr(inv_perm), _ptr(device_status),
+                                    _stream(stream)), "moe_permute_noalloc")
+    return out
 
 
 def moe_expert_ffn(shape: Shape, x, perm, offsets, counts, W_gate, W_up, W_down,

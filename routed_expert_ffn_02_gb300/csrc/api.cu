@@ -22,6 +22,17 @@ moe_status fail(moe_status st, const char* fmt, ...) {
     return st;
 }
 
+}  // namespace
+
+void moe::set_last_error(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+}
+
+namespace {
+
 moe_status ok() {
     g_err[0] = '\0';
     return MOE_OK;

@@ -94,6 +94,9 @@ cudaError_t launch_combine(const __nv_bfloat16* y_sorted, const int32_t* inv_per
                            const float* gates, int T, int k, int H,
                            __nv_bfloat16* out, int num_sms, cudaStream_t s);
 
+// Sets the calling thread's moe_last_error() message (printf format).
+void set_last_error(const char* fmt, ...);
+
 // Records a device-side condition in the workspace status word (first one wins).
 __device__ __forceinline__ void set_status(WsHeader* hdr, int code) {
     atomicCAS(&hdr->status, 0, code);

@@ -1,0 +1,96 @@
+// permute_noalloc.cu -- moe_permute_noalloc: the route-list kernels with
+// their scratch in a fixed device array owned by the library, for callers
+// that cannot allocate device memory.
+//
+// Who needs it: a serving process that hands every byte of HBM to the expert
+// weights and the KV cache up front and keeps no pool to carve a workspace
+// from, and host code that must not call cudaMalloc on its hot path because
+// cudaMalloc can synchronise the whole device and stall the other streams.
+// Such callers pass only inputs and outputs; the histogram and scan scratch
+// lives in `g_permute_scratch` below.
+//
+// Costs and rules of the shared array:
+//   * Every GPU that loads libmoe holds the array (kScratchBytes, about
+//     1 MiB) until the process exits.
+//   * All calls on a device share it and it keeps the previous call's
+//     contents; each call clears the status word before its kernels run, and
+//     the kernels overwrite every other byte they read.
+//   * Calls whose kernels overlap on the GPU (different streams without
+//     ordering between them) race on the array and give wrong results.
+//   * Host code cannot use the array's name as a device address (on the host
+//     it names a host-side shadow).  The device address is looked up once per
+//     device with cudaGetSymbolAddress, with that device current, by the
+//     first call made on it; make that first call before any stream capture.
+#include <mutex>
+
+#include "moe_internal.cuh"
+
+using namespace moe;
+
+namespace {
+
+constexpr int64_t kNoallocMaxSlots = 262144;   // T * k
+constexpr int64_t kNoallocMaxChunks = kNoallocMaxSlots / kPermChunk;
+constexpr size_t kScratchInts = (size_t)2 * kNoallocMaxChunks * kMaxE;
+constexpr size_t kScratchBytes = sizeof(WsHeader) + kScratchInts * sizeof(int32_t);
+
+// [WsHeader | chunk_hist | chunk_base]
+static __device__ __align__(256) unsigned char g_permute_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+}  // namespace
+
+extern "C" moe_status moe_permute_noalloc(const int32_t* topk_idx, int32_t T, int32_t E,
+                                          int32_t k, int32_t* counts, int32_t* offsets,
+                                          int32_t* perm, int32_t* inv_perm,
+                                          int32_t* device_status, moe_stream_t stream) {
+    auto fail = [](moe_status st, const char* msg) {
+        set_last_error("moe_permute_noalloc: %s", msg);
+        return st;
+    };
+    set_last_error("");
+    if (T < 0 || E < 1 || E > kMaxE || k < 1 || k > kMaxK || k > E)
+        return fail(MOE_ERR_INVALID_ARG, "T, E or k outside the limits of moe_permute");
+    const int64_t P = (int64_t)T * k;
+    if (P > kNoallocMaxSlots)
+        return fail(MOE_ERR_UNSUPPORTED,
+                    "T*k exceeds the 262144 slots its fixed scratch holds; use moe_permute");
+    if (!counts || !offsets || (P > 0 && (!topk_idx || !perm || !inv_perm)))
+        return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return fail(MOE_ERR_CUDA, "cudaGetDevice failed");
+    void* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_scratch_addr[dev]) {
+            void* p = nullptr;
+            const cudaError_t e = cudaGetSymbolAddress(&p, g_permute_scratch);
+            if (e != cudaSuccess || !p) return fail(MOE_ERR_CUDA, cudaGetErrorString(e));
+            g_scratch_addr[dev] = p;
+        }
+        base = g_scratch_addr[dev];
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    WsHeader* hdr = static_cast<WsHeader*>(base);
+    int32_t* chunk_hist = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(base) +
+                                                     sizeof(WsHeader));
+    const int64_t nch = (P + kPermChunk - 1) / kPermChunk;
+    int32_t* chunk_base = chunk_hist + nch * E;
+
+    // The status word must start at zero; everything else is overwritten.
+    if (cudaMemsetAsync(&hdr->status, 0, sizeof(int32_t), s) != cudaSuccess)
+        return fail(MOE_ERR_CUDA, "cudaMemsetAsync failed");
+    cudaError_t e = launch_permute(topk_idx, T, E, k, counts, offsets, perm, inv_perm,
+                                   chunk_hist, chunk_base, hdr, nullptr, s);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, cudaGetErrorString(e));
+    if (device_status &&
+        cudaMemcpyAsync(device_status, &hdr->status, sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                        s) != cudaSuccess)
+        return fail(MOE_ERR_CUDA, "cudaMemcpyAsync of the status word failed");
+    return MOE_OK;
+}
