@@ -42,7 +42,8 @@
  *     is recorded in the workspace's status word, read with
  *     moe_workspace_status().
  *   - Limits: 1 <= k <= min(E, 8); 1 <= E <= 1024; T >= 0 with T*k < 2^31;
- *     H and I positive multiples of 256; 0 <= fat_threshold <= 33 (experts
+ *     H and I positive multiples of 256, at most 16384 (MOE_ERR_UNSUPPORTED
+ *     above); 0 <= fat_threshold <= 33 (experts
  *     with fewer slots than the threshold take the weight-streaming path,
  *     which holds at most 32 slots per expert).
  *   - Preconditions not checked: logits hold no NaN and no +inf, and each

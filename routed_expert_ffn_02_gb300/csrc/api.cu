@@ -94,6 +94,8 @@ moe_status check_shape(const moe_shape* sh) {
     if (st != MOE_OK) return st;
     if (sh->H < 256 || sh->H % 256) return fail(MOE_ERR_INVALID_ARG, "H = %d is not a positive multiple of 256", sh->H);
     if (sh->I < 256 || sh->I % 256) return fail(MOE_ERR_INVALID_ARG, "I = %d is not a positive multiple of 256", sh->I);
+    if (sh->H > kMaxHidden || sh->I > kMaxHidden)
+        return fail(MOE_ERR_UNSUPPORTED, "H and I are limited to %d", kMaxHidden);
     if (sh->fat_threshold < 0 || sh->fat_threshold > kThinMaxTokens + 1)
         return fail(MOE_ERR_INVALID_ARG, "fat_threshold = %d outside [0, %d]", sh->fat_threshold,
                     kThinMaxTokens + 1);
@@ -119,7 +121,7 @@ int64_t rows_alloc(int64_t P) { return std::max<int64_t>(P, kTileM); }
 struct FfnBufs {
     WsHeader* hdr;
     FatTile* tiles;
-    int32_t* thin;
+    ThinUnit* units;
     __nv_bfloat16* x_sorted;
     __nv_bfloat16* h;
 };
@@ -129,7 +131,7 @@ struct FwdBufs {
     int32_t *idx, *counts, *offsets, *perm, *inv_perm, *chunk;
     float* gates;
     FatTile* tiles;
-    int32_t* thin;
+    ThinUnit* units;
     __nv_bfloat16* xy;   // x_sorted, later reused for y_sorted
     __nv_bfloat16* h;
 };
@@ -139,7 +141,7 @@ size_t carve_ffn(const moe_shape* sh, void* ws, FfnBufs* b) {
     Carver c(ws);
     b->hdr = c.take<WsHeader>(1);
     b->tiles = c.take<FatTile>((size_t)max_fat_tiles(P, sh->E));
-    b->thin = c.take<int32_t>((size_t)sh->E);
+    b->units = c.take<ThinUnit>((size_t)max_thin_units(sh->E, thin_unit_tokens(sh->H, sh->I)));
     b->x_sorted = c.take<__nv_bfloat16>((size_t)(rows_alloc(P) * sh->H));
     b->h = c.take<__nv_bfloat16>((size_t)(rows_alloc(P) * sh->I));
     return align_up(c.off, 256);
@@ -157,7 +159,7 @@ size_t carve_fwd(const moe_shape* sh, void* ws, FwdBufs* b) {
     b->inv_perm = c.take<int32_t>((size_t)P);
     b->chunk = c.take<int32_t>(permute_scratch_ints(P, sh->E));
     b->tiles = c.take<FatTile>((size_t)max_fat_tiles(P, sh->E));
-    b->thin = c.take<int32_t>((size_t)sh->E);
+    b->units = c.take<ThinUnit>((size_t)max_thin_units(sh->E, thin_unit_tokens(sh->H, sh->I)));
     b->xy = c.take<__nv_bfloat16>((size_t)(rows_alloc(P) * sh->H));
     b->h = c.take<__nv_bfloat16>((size_t)(rows_alloc(P) * sh->I));
     return align_up(c.off, 256);
@@ -201,7 +203,7 @@ cudaError_t mark(cudaEvent_t* ev, int i, cudaStream_t s) {
 
 // Expert stage shared by moe_expert_ffn and moe_forward.  `fat_bound` is an
 // upper bound of any expert's count (no GEMM launch when it is below the
-// threshold).
+// threshold; it also sizes the streaming kernels' activation buffers).
 moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bfloat16* x,
                        const int32_t* perm, const int32_t* offsets, const int32_t* counts,
                        const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
@@ -221,15 +223,15 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
                                      dev.num_sms, s), "grouped GEMM gate/up");
     CUDA_TRY(mark(ev, kEvGemmGateUp, s), "cudaEventRecord");
     if (any_thin)
-        CUDA_TRY(launch_thin_gate_up(x, perm, offsets, counts, sh->k, sh->H, sh->I, Wg, Wu,
-                                     plan, h, dev.num_sms, s), "thin gate/up");
+        CUDA_TRY(launch_thin_gate_up(x, perm, sh->k, sh->H, sh->I, Wg, Wu, plan, fat_bound, h,
+                                     dev.num_sms, s), "thin gate/up");
     CUDA_TRY(mark(ev, kEvThinGateUp, s), "cudaEventRecord");
     if (any_fat)
         CUDA_TRY(launch_gemm_down(h, ra, Wd, sh->E, sh->H, sh->I, plan, y, dev.num_sms, s),
                  "grouped GEMM down");
     CUDA_TRY(mark(ev, kEvGemmDown, s), "cudaEventRecord");
     if (any_thin)
-        CUDA_TRY(launch_thin_down(h, offsets, counts, sh->H, sh->I, Wd, plan, y, dev.num_sms, s),
+        CUDA_TRY(launch_thin_down(h, sh->H, sh->I, Wd, plan, fat_bound, y, dev.num_sms, s),
                  "thin down");
     CUDA_TRY(mark(ev, kEvThinDown, s), "cudaEventRecord");
     return MOE_OK;
@@ -302,7 +304,8 @@ moe_status moe_expert_ffn(const moe_shape* shape, const moe_bf16* x, const int32
     DeviceInfo dev;
     if ((st = device_info(&dev)) != MOE_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    Plan plan{b.tiles, b.thin, b.hdr, shape->fat_threshold};
+    Plan plan{b.tiles, b.units, b.hdr, shape->fat_threshold,
+              thin_unit_tokens(shape->H, shape->I)};
     CUDA_TRY(launch_plan(counts, offsets, shape->E, plan, s), "plan");
     st = run_experts(shape, dev, (const __nv_bfloat16*)x, perm, offsets, counts,
                      (const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
@@ -356,7 +359,8 @@ static moe_status forward_impl(const moe_shape* shape, const float* logits, cons
     CUDA_TRY(mark(ev, kEvStart, s), "cudaEventRecord");
     CUDA_TRY(launch_route(logits, T, E, k, idx, g, s), "route");
     CUDA_TRY(mark(ev, kEvRoute, s), "cudaEventRecord");
-    Plan plan{b.tiles, b.thin, b.hdr, shape->fat_threshold};
+    Plan plan{b.tiles, b.units, b.hdr, shape->fat_threshold,
+              thin_unit_tokens(shape->H, shape->I)};
     const int64_t P = (int64_t)T * k;
     const int64_t nch = (P + kPermChunk - 1) / kPermChunk;
     CUDA_TRY(launch_permute(idx, T, E, k, b.counts, b.offsets, b.perm, b.inv_perm, b.chunk,

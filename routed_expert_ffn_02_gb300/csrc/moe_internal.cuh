@@ -17,13 +17,15 @@ constexpr int kMaxE = 1024;          // experts per layer
 constexpr int kThinMaxTokens = 32;   // slots one weight-streaming expert may hold
 constexpr int kPermChunk = 2048;     // slots per block in the route-list kernels
 constexpr int kTileM = 128;          // rows (slots) per grouped-GEMM tile
+constexpr int kMaxHidden = 16384;    // H and I (a weight-streaming stage holds a row)
 
 // First 256 bytes of every workspace.
 struct WsHeader {
     int32_t status;        // moe_status recorded by kernels (sticky)
     int32_t n_fat_tiles;   // grouped-GEMM row tiles built by the planner
-    int32_t n_thin;        // experts on the weight-streaming path
-    int32_t reserved[61];
+    int32_t n_thin;        // work units on the weight-streaming path
+    int32_t thin_weight;   // sum of thin_unit_cost over those units
+    int32_t reserved[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -36,17 +38,39 @@ struct FatTile {
     int32_t pad;
 };
 
+// One weight-streaming work unit: up to `unit_tokens` consecutive sorted slots
+// [row0, row0 + n) of expert `expert`.  An expert with more slots than a
+// unit holds is split into several units, each streaming the expert's weights.
+struct ThinUnit {
+    int32_t expert;
+    int32_t row0;
+    int32_t n;
+    int32_t cost_before;   // sum of thin_unit_cost over the preceding units
+};
+
+// Relative cost of one weight row of a unit with n slots on the streaming
+// path: flat while the row is bound by its HBM read, then growing with the
+// FMAs (used to split units' rows evenly over CTAs).
+__host__ __device__ inline int thin_unit_cost(int n) { return (n < 4 ? 4 : n) + 2; }
+
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Planner outputs (the split of experts between the two expert paths).
 struct Plan {
-    FatTile* tiles;     // [max_fat_tiles(P, E)]
-    int32_t* thin;      // [E] experts on the weight-streaming path, ascending
+    FatTile* tiles;      // [max_fat_tiles(P, E)]
+    ThinUnit* units;     // [max_thin_units(E, unit_tokens)], expert-major
     WsHeader* hdr;
     int32_t fat_threshold;
+    int32_t unit_tokens; // slots per weight-streaming unit (thin_unit_tokens)
 };
 
 inline int64_t max_fat_tiles(int64_t P, int E) { return P / kTileM + E + 1; }
+inline int64_t max_thin_units(int E, int unit_tokens) {
+    return (int64_t)E * ((kThinMaxTokens + unit_tokens - 1) / unit_tokens);
+}
+// Slots per weight-streaming unit for these sizes (their activations are
+// staged in shared memory together).
+int thin_unit_tokens(int H, int I);
 
 // Launchers (all asynchronous on `s`; they return the launch's cudaError_t).
 cudaError_t launch_route(const float* logits, int T, int E, int k,
@@ -67,17 +91,16 @@ cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* perm, int k,
                           int H, const Plan& plan, __nv_bfloat16* x_sorted,
                           int num_sms, cudaStream_t s);
 
-cudaError_t launch_thin_gate_up(const __nv_bfloat16* x, const int32_t* perm,
-                                const int32_t* offsets, const int32_t* counts,
-                                int k, int H, int I, const __nv_bfloat16* Wg,
-                                const __nv_bfloat16* Wu, const Plan& plan,
-                                __nv_bfloat16* h, int num_sms, cudaStream_t s);
+// max_slots: an upper bound of any expert's slot count (sizes the staged
+// activation buffer; units never hold more than plan.unit_tokens).
+cudaError_t launch_thin_gate_up(const __nv_bfloat16* x, const int32_t* perm, int k, int H,
+                                int I, const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
+                                const Plan& plan, int64_t max_slots, __nv_bfloat16* h,
+                                int num_sms, cudaStream_t s);
 
-cudaError_t launch_thin_down(const __nv_bfloat16* h, const int32_t* offsets,
-                             const int32_t* counts, int H, int I,
-                             const __nv_bfloat16* Wd, const Plan& plan,
-                             __nv_bfloat16* y_sorted, int num_sms,
-                             cudaStream_t s);
+cudaError_t launch_thin_down(const __nv_bfloat16* h, int H, int I, const __nv_bfloat16* Wd,
+                             const Plan& plan, int64_t max_slots, __nv_bfloat16* y_sorted,
+                             int num_sms, cudaStream_t s);
 
 // Grouped GEMMs on tcgen05.  gate_up: h = silu(A Wg^T) * (A Wu^T) for the
 // fat tiles, A = x_sorted [rows_alloc, H].  down: y = h Wd^T, A = h.

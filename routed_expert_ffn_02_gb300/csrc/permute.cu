@@ -68,21 +68,24 @@ __device__ int block_exclusive_scan(int* a, int n, int* ws) {
 }
 
 // Planner: fat experts (count >= threshold, count > 0) get ceil(count/128)
-// row tiles; thin experts (0 < count < threshold) go on the thin list.
+// row tiles; thin experts (0 < count < threshold) get ceil(count/unit_tokens)
+// weight-streaming units, each with the running sum of unit costs before it
+// (thin_unit_cost) so the streaming kernels can split rows evenly by cost.
 // cnt/off: shared copies of counts/offsets; ta, tb: shared int[E] scratch.
 template <int NT>
 __device__ void block_plan(const int* cnt, const int* off, int E, const Plan& plan,
                            int* ta, int* tb, int* ws) {
     const int thr = plan.fat_threshold;
+    const int nu = plan.unit_tokens;
     for (int e = threadIdx.x; e < E; e += NT) {
         const int c = cnt[e];
         const bool fat = c > 0 && c >= thr;
         ta[e] = fat ? (c + kTileM - 1) / kTileM : 0;
-        tb[e] = (c > 0 && c < thr) ? 1 : 0;
+        tb[e] = (c > 0 && c < thr) ? (c + nu - 1) / nu : 0;
     }
     __syncthreads();
     const int n_tiles = block_exclusive_scan<NT>(ta, E, ws);
-    const int n_thin = block_exclusive_scan<NT>(tb, E, ws);
+    const int n_units = block_exclusive_scan<NT>(tb, E, ws);
     for (int e = threadIdx.x; e < E; e += NT) {
         const int c = cnt[e];
         if (c > 0 && c >= thr) {
@@ -95,13 +98,38 @@ __device__ void block_plan(const int* cnt, const int* off, int E, const Plan& pl
                 ft.pad = 0;
                 plan.tiles[ta[e] + i] = ft;
             }
-        } else if (c > 0) {
-            plan.thin[tb[e]] = e;
+        }
+    }
+    // Unit costs: reuse ta as each thin expert's total cost, scanned.
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += NT) {
+        const int c = cnt[e];
+        int w = 0;
+        if (c > 0 && c < thr)
+            for (int i = 0; i * nu < c; ++i) w += thin_unit_cost(min(nu, c - i * nu));
+        ta[e] = w;
+    }
+    __syncthreads();
+    const int weight = block_exclusive_scan<NT>(ta, E, ws);
+    for (int e = threadIdx.x; e < E; e += NT) {
+        const int c = cnt[e];
+        if (c > 0 && c < thr) {
+            int before = ta[e];
+            for (int i = 0; i * nu < c; ++i) {
+                ThinUnit u;
+                u.expert = e;
+                u.row0 = off[e] + i * nu;
+                u.n = min(nu, c - i * nu);
+                u.cost_before = before;
+                before += thin_unit_cost(u.n);
+                plan.units[tb[e] + i] = u;
+            }
         }
     }
     if (threadIdx.x == 0) {
         plan.hdr->n_fat_tiles = n_tiles;
-        plan.hdr->n_thin = n_thin;
+        plan.hdr->n_thin = n_units;
+        plan.hdr->thin_weight = weight;
     }
 }
 

@@ -3,29 +3,105 @@
 //
 // In decode only a handful of experts per layer are touched per token
 // (dsv41-flash-offload wiki, PCIe paragraph); each touched expert's weights
-// are read from HBM once and applied to all (<= 32) of its slots.  The work is
-// memory-bound: one warp owns one weight row, streams it with 16-byte
-// coalesced loads, keeps one fp32 accumulator per slot in registers and
-// finishes with warp-shuffle reductions.
+// are read from HBM once and applied to all of its slots.  The work is
+// memory-bound for few slots and CUDA-core-bound for many; the kernel keeps
+// HBM busy and the FMA pipes fed:
+//
+//   * Work units (from the planner) hold up to `unit_tokens` consecutive
+//     sorted slots of one expert; their activations (x rows for gate/up, h
+//     rows for down) are staged together in shared memory.  A unit's weight
+//     rows are split into items of R consecutive rows: one 16 KB slot, one
+//     contiguous range in HBM.
+//   * One CTA per SM owns a contiguous range of items whose total cost is an
+//     equal share of the layer's (the planner prices a row by its unit's slot
+//     count: flat while HBM-bound, growing with the FMAs).
+//   * Warp-specialised: producer lanes stream the items' weight rows into a
+//     ring of shared-memory slots with bulk copies on the TMA engine
+//     (cp.async.bulk + mbarrier) -- two producers for gate/up (gate rows and up
+//     rows), since one issuing thread sustains only so many copies per second
+//     -- and the first producer also stages each unit's activations once the
+//     consumers have released the previous unit's.  Producers sleep in
+//     try_wait while the ring is full.  The other warps consume slots
+//     round-robin.
+//   * Slot protocol: a consumer waits until the slot's previous round has been
+//     released, then for the current round to land; with more slots than
+//     consumers this makes every parity wait unambiguous.
+//   * A consumer lane covers the 16-byte vectors lane, lane+32, ... of a row.
+//     With few slots (<= 4) it copies its share of the whole slot into
+//     registers and releases the slot at once, so the ring refills while it
+//     computes.  Products are mixed-precision FMAs (fma.rn.f32.bf16: bf16
+//     operands straight from the staged data, fp32 accumulators, no
+//     conversions) spread over enough independent accumulators to cover the
+//     FMA latency; the warp finishes each row with shuffle reductions and
+//     lane t writes slot t's result.
 //
 //   gate/up: h[p, i] = bf16( silu(Wg[e,i,:] . x_t) * (Wu[e,i,:] . x_t) )
 //   down:    y[p, r] = bf16( Wd[e,r,:] . h[p, :] )
 // for every sorted position p of expert e (token t = perm[p] / k).
+//
+// Waits are bounded; on expiry the kernel records MOE_ERR_TIMEOUT, the
+// producer waits (bounded) for its outstanding copies, and the CTA returns.
+#include <algorithm>
+
 #include "moe_internal.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kWarpsPerBlock = 8;
+using namespace ptx;
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
-    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 t = __bfloat1622float2(p[i]);
-        f[2 * i] = t.x;
-        f[2 * i + 1] = t.y;
+constexpr int kWarps = 8;                      // producers + consumers
+constexpr int kThreads = 32 * kWarps;
+constexpr int kMaxSlots = 16;
+constexpr int kSmemBudget = 224 * 1024;
+constexpr int kActBudget = 96 * 1024;          // activation buffer
+constexpr int kStageTarget = 16384;            // bytes per weight slot
+constexpr int kMaxUnitTokens = 16;
+constexpr int kRegSlots = 4;                   // register-cached path up to this many slots
+
+// ---- shared loads, mixed-precision FMA ---------------------------------------
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// The two bf16 halves of a 32-bit word as 16-bit registers.
+__device__ __forceinline__ void split_bf16x2(uint32_t w, unsigned short& lo, unsigned short& hi) {
+    asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(w));
+}
+// acc += w * x with bf16 operands, exact products, fp32 accumulation.
+__device__ __forceinline__ void fma_bf16(float& acc, unsigned short w, unsigned short x) {
+    asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(acc) : "h"(w), "h"(x));
+}
+
+struct Bf16x8 {   // eight bf16 values as 16-bit registers
+    unsigned short h[8];
+    __device__ __forceinline__ explicit Bf16x8(const uint4& v) {
+        split_bf16x2(v.x, h[0], h[1]);
+        split_bf16x2(v.y, h[2], h[3]);
+        split_bf16x2(v.z, h[4], h[5]);
+        split_bf16x2(v.w, h[6], h[7]);
     }
+};
+
+// Independent accumulators per slot and matrix: at least eight chains per
+// warp to cover the FMA latency.  Divides 8 (element q goes to chain q % P).
+template <int N>
+struct Chains {
+    static constexpr int P = N >= 8 ? 1 : (N >= 4 ? 2 : (N >= 2 ? 4 : 8));
+};
+
+template <int P>
+__device__ __forceinline__ float sum_chains(const float (&a)[P]) {
+    float s = a[0];
+#pragma unroll
+    for (int i = 1; i < P; ++i) s += a[i];
+    return s;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -34,199 +110,597 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-__device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-    return r;
-}
-
-// One row i of expert e for its n (<= NT) slots.  xrow[t] = token row offsets
-// (in uint4 units), held in shared memory by the calling warp.
-template <int NT>
-__device__ __forceinline__ void gate_up_row(const uint4* __restrict__ wg,
-                                            const uint4* __restrict__ wu,
-                                            const uint4* __restrict__ x,
-                                            const int64_t* xrow, int n, int vec,
-                                            float (&g)[NT], float (&u)[NT]) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int t = 0; t < NT; ++t) { g[t] = 0.f; u[t] = 0.f; }
-#pragma unroll 2
-    for (int v = lane; v < vec; v += 32) {
-        float fg[8], fu[8];
-        bf16x8_to_f32(ldg_stream(wg + v), fg);
-        bf16x8_to_f32(ldg_stream(wu + v), fu);
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            if (t < n) {
-                float fx[8];
-                bf16x8_to_f32(__ldg(x + xrow[t] + v), fx);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    g[t] = fmaf(fg[q], fx[q], g[t]);
-                    u[t] = fmaf(fu[q], fx[q], u[t]);
-                }
-            }
-        }
-    }
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-        if (t < n) {
-            g[t] = warp_sum(g[t]);
-            u[t] = warp_sum(u[t]);
-        }
-    }
-}
-
-template <int NT>
-__device__ __forceinline__ void down_row(const uint4* __restrict__ wd,
-                                         const uint4* __restrict__ h,
-                                         int64_t hrow0, int n, int vec,
-                                         float (&acc)[NT]) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
-#pragma unroll 2
-    for (int v = lane; v < vec; v += 32) {
-        float fw[8];
-        bf16x8_to_f32(ldg_stream(wd + v), fw);
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            if (t < n) {
-                float fh[8];
-                bf16x8_to_f32(__ldg(h + (hrow0 + t) * vec + v), fh);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) acc[t] = fmaf(fw[q], fh[q], acc[t]);
-            }
-        }
-    }
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-        if (t < n) acc[t] = warp_sum(acc[t]);
-}
-
 __device__ __forceinline__ float silu_mul(float g, float u) {
     return g / (1.0f + __expf(-g)) * u;
 }
 
-template <int NT>
-__device__ __forceinline__ void gate_up_item(const uint4* wg, const uint4* wu,
-                                             const uint4* x, const int64_t* xrow,
-                                             int n, int vec, __nv_bfloat16* hcol,
-                                             int64_t ldh) {
-    float g[NT], u[NT];
-    gate_up_row<NT>(wg, wu, x, xrow, n, vec, g, u);
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-        if (t < n && lane == t) hcol[t * ldh] = __float2bfloat16_rn(silu_mul(g[t], u[t]));
-}
+// ---- shared-memory layout and pipeline ------------------------------------
 
-template <int NT>
-__device__ __forceinline__ void down_item(const uint4* wd, const uint4* h,
-                                          int64_t hrow0, int n, int vec,
-                                          __nv_bfloat16* ycol, int64_t ldy) {
-    float acc[NT];
-    down_row<NT>(wd, h, hrow0, n, vec, acc);
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-        if (t < n && lane == t) ycol[t * ldy] = __float2bfloat16_rn(acc[t]);
-}
+// [slots x stage_bytes weight ring][activation buffer][barriers]
+struct Smem {
+    uint32_t base;       // shared addresses
+    uint32_t act;
+    uint32_t bars;
+    int stage_bytes;
+    int slots;
+    __device__ uint32_t buf(int s) const { return base + (uint32_t)(s * stage_bytes); }
+    __device__ uint32_t full(int s) const { return bars + 8u * s; }
+    __device__ uint32_t empty(int s) const { return bars + 8u * (kMaxSlots + s); }
+    __device__ uint32_t act_full() const { return bars + 8u * (2 * kMaxSlots); }
+    __device__ uint32_t act_free() const { return bars + 8u * (2 * kMaxSlots + 1); }
+};
 
-// Work item = (thin expert q, weight row i); items are spread over all warps
-// of a persistent grid so every SM streams weights.
-__global__ void __launch_bounds__(32 * kWarpsPerBlock)
-thin_gate_up_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
-                    const int32_t* __restrict__ offsets,
-                    const int32_t* __restrict__ counts, int k, int H, int I,
-                    const uint4* __restrict__ Wg, const uint4* __restrict__ Wu,
-                    const int32_t* __restrict__ thin, const WsHeader* __restrict__ hdr,
-                    __nv_bfloat16* __restrict__ h) {
-    __shared__ int64_t xrow_s[kWarpsPerBlock][kThinMaxTokens];
-    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-    const int64_t warp = (int64_t)blockIdx.x * kWarpsPerBlock + wib;
-    const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerBlock;
-    const int64_t items = (int64_t)hdr->n_thin * I;
-    const int vec = H / 8;
-    int cur_q = -1;
-    int e = 0, n = 0, row0 = 0;
-    for (int64_t it = warp; it < items; it += nwarps) {
-        const int q = (int)(it / I);
-        const int i = (int)(it % I);
-        if (q != cur_q) {
-            cur_q = q;
-            e = thin[q];
-            n = min(counts[e], kThinMaxTokens);
-            row0 = offsets[e];
-            __syncwarp();
-            if (lane < n) xrow_s[wib][lane] = (int64_t)(perm[row0 + lane] / k) * vec;
-            __syncwarp();
+__device__ __forceinline__ Smem smem_setup(uint8_t* smem, int stage_bytes, int slots,
+                                           int act_bytes, int producers, int consumers) {
+    Smem m;
+    m.base = smem_u32(smem);
+    m.stage_bytes = stage_bytes;
+    m.slots = slots;
+    m.act = m.base + (uint32_t)(slots * stage_bytes);
+    m.bars = m.act + (uint32_t)act_bytes;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < slots; ++s) {
+            mbar_init(m.full(s), producers);
+            mbar_init(m.empty(s), 1);
         }
-        const uint4* wg = Wg + ((int64_t)e * I + i) * vec;
-        const uint4* wu = Wu + ((int64_t)e * I + i) * vec;
-        __nv_bfloat16* hcol = h + (int64_t)row0 * I + i;
-        const int64_t* xr = xrow_s[wib];
-        if (n <= 1) gate_up_item<1>(wg, wu, x, xr, n, vec, hcol, I);
-        else if (n <= 2) gate_up_item<2>(wg, wu, x, xr, n, vec, hcol, I);
-        else if (n <= 4) gate_up_item<4>(wg, wu, x, xr, n, vec, hcol, I);
-        else if (n <= 8) gate_up_item<8>(wg, wu, x, xr, n, vec, hcol, I);
-        else if (n <= 16) gate_up_item<16>(wg, wu, x, xr, n, vec, hcol, I);
-        else gate_up_item<32>(wg, wu, x, xr, n, vec, hcol, I);
+        mbar_init(m.act_full(), 1);
+        mbar_init(m.act_free(), consumers);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    return m;
+}
+
+struct Range {
+    int beg, cnt;          // items [beg, beg + cnt)
+    int u_first, u_last;   // units they span (u_last < u_first when cnt == 0)
+};
+
+// First item whose cumulative cost reaches c: units have ipe items each, all
+// of cost thin_unit_cost(n); units[u].cost_before is the per-item cost of the
+// units before u.
+__device__ __forceinline__ int item_at(const ThinUnit* units, int n_units, int ipe, int64_t c) {
+    int lo = 0, hi = n_units - 1;   // largest u with ipe * cost_before <= c
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)units[mid].cost_before * ipe <= c) lo = mid;
+        else hi = mid - 1;
+    }
+    const int w = thin_unit_cost(units[lo].n);
+    const int64_t off = c - (int64_t)units[lo].cost_before * ipe;
+    const int64_t k = (off + w - 1) / w;
+    return lo * ipe + (int)(k < ipe ? k : ipe);
+}
+
+// This CTA's contiguous share of the items, of (about) equal total cost.
+__device__ __forceinline__ Range cta_range(const ThinUnit* units, const WsHeader* hdr, int ipe) {
+    Range r;
+    const int n_units = hdr->n_thin;
+    if (n_units <= 0) {
+        r.beg = r.cnt = 0;
+        r.u_first = 0;
+        r.u_last = -1;
+        return r;
+    }
+    const int64_t total = (int64_t)hdr->thin_weight * ipe;
+    const int64_t c0 = total * blockIdx.x / gridDim.x;
+    const int64_t c1 = total * (blockIdx.x + 1) / gridDim.x;
+    r.beg = item_at(units, n_units, ipe, c0);
+    const int end = blockIdx.x + 1 == gridDim.x ? n_units * ipe : item_at(units, n_units, ipe, c1);
+    r.cnt = end - r.beg;
+    r.u_first = r.beg / ipe;
+    r.u_last = r.cnt > 0 ? (r.beg + r.cnt - 1) / ipe : r.u_first - 1;
+    return r;
+}
+
+// All lanes of a warp wait (bounded, convergent) for the phase with the given
+// parity.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+    const bool ok = mbar_wait(bar, parity);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Producer (one lane): streams the range's items through the weight ring
+// (copy_item) and, if it is the `stager`, stages each unit's activations
+// (copy_act) once the consumers have released the previous unit's.  While a
+// slot is still in use the lane sleeps in try_wait.  Returns false on a timeout.
+template <typename ItemFn, typename ActFn>
+__device__ bool produce(const Smem& m, const Range& rg, bool stager, ItemFn copy_item,
+                        ActFn copy_act) {
+    if (rg.cnt <= 0) return true;
+    int last_round[kMaxSlots];
+    for (int s = 0; s < kMaxSlots; ++s) last_round[s] = -1;
+    const int n_units = stager ? rg.u_last - rg.u_first + 1 : 0;
+    int act_issued = 0;                       // units whose activations are staged
+    if (stager) {
+        copy_act(rg.u_first, m.act, m.act_full());
+        act_issued = 1;
+    }
+    auto try_stage = [&]() {   // never blocks
+        if (act_issued < n_units &&
+            mbar_test_wait(m.act_free(), (uint32_t)((act_issued - 1) & 1))) {
+            copy_act(rg.u_first + act_issued, m.act, m.act_full());
+            ++act_issued;
+        }
+    };
+    bool ok = true;
+    int slot = 0, round = 0;
+    for (int seq = 0; ok && seq < rg.cnt; ++seq) {
+        if (round > 0) {
+            const uint32_t par = (uint32_t)((round - 1) & 1);
+            const long long start = clock64();
+            while (!mbar_try_wait_sleep(m.empty(slot), par, 2000)) {
+                try_stage();
+                if (clock64() - start > kWaitCycles) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok) break;
+        }
+        copy_item(rg.beg + seq, m.buf(slot), m.full(slot));
+        last_round[slot] = round;
+        try_stage();
+        if (++slot == m.slots) {
+            slot = 0;
+            ++round;
+        }
+    }
+    while (ok && act_issued < n_units) {
+        if (!mbar_wait(m.act_free(), (uint32_t)((act_issued - 1) & 1))) {
+            ok = false;
+            break;
+        }
+        copy_act(rg.u_first + act_issued, m.act, m.act_full());
+        ++act_issued;
+    }
+    if (!ok) {
+        // Let the copies already issued land before the CTA exits.
+        for (int s = 0; s < m.slots; ++s)
+            if (last_round[s] >= 0) (void)mbar_wait(m.full(s), (uint32_t)(last_round[s] & 1));
+        if (act_issued > 0) (void)mbar_wait(m.act_full(), (uint32_t)((act_issued - 1) & 1));
+    }
+    return ok;
+}
+
+// Called by all lanes of a consumer warp once they are done reading a slot.
+__device__ __forceinline__ void release_slot(const Smem& m, int slot) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(m.empty(slot));
+}
+
+// Calls f.template operator()<N>() for the runtime slot count n in [1, 16].
+template <typename F>
+__device__ __forceinline__ void with_slots(int n, F&& f) {
+    switch (n) {
+        case 1: f.template operator()<1>(); break;
+        case 2: f.template operator()<2>(); break;
+        case 3: f.template operator()<3>(); break;
+        case 4: f.template operator()<4>(); break;
+        case 5: f.template operator()<5>(); break;
+        case 6: f.template operator()<6>(); break;
+        case 7: f.template operator()<7>(); break;
+        case 8: f.template operator()<8>(); break;
+        case 9: f.template operator()<9>(); break;
+        case 10: f.template operator()<10>(); break;
+        case 11: f.template operator()<11>(); break;
+        case 12: f.template operator()<12>(); break;
+        case 13: f.template operator()<13>(); break;
+        case 14: f.template operator()<14>(); break;
+        case 15: f.template operator()<15>(); break;
+        default: f.template operator()<16>(); break;
     }
 }
 
-__global__ void __launch_bounds__(32 * kWarpsPerBlock)
-thin_down_kernel(const uint4* __restrict__ h, const int32_t* __restrict__ offsets,
-                 const int32_t* __restrict__ counts, int H, int I,
-                 const uint4* __restrict__ Wd, const int32_t* __restrict__ thin,
-                 const WsHeader* __restrict__ hdr, __nv_bfloat16* __restrict__ y) {
-    const int wib = threadIdx.x >> 5;
-    const int64_t warp = (int64_t)blockIdx.x * kWarpsPerBlock + wib;
-    const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerBlock;
-    const int64_t items = (int64_t)hdr->n_thin * H;
-    const int vec = I / 8;
-    for (int64_t it = warp; it < items; it += nwarps) {
-        const int q = (int)(it / H);
-        const int r = (int)(it % H);
-        const int e = thin[q];
-        const int n = min(counts[e], kThinMaxTokens);
-        const int row0 = offsets[e];
-        const uint4* wd = Wd + ((int64_t)e * H + r) * vec;
-        __nv_bfloat16* ycol = y + (int64_t)row0 * H + r;
-        if (n <= 1) down_item<1>(wd, h, row0, n, vec, ycol, H);
-        else if (n <= 2) down_item<2>(wd, h, row0, n, vec, ycol, H);
-        else if (n <= 4) down_item<4>(wd, h, row0, n, vec, ycol, H);
-        else if (n <= 8) down_item<8>(wd, h, row0, n, vec, ycol, H);
-        else if (n <= 16) down_item<16>(wd, h, row0, n, vec, ycol, H);
-        else down_item<32>(wd, h, row0, n, vec, ycol, H);
+// Consumer warp c of nc.  For each unit of the range: wait for its
+// activations, then for the warp's items of that unit (seq = c mod nc) wait
+// for the slot and run item.template operator()<N>(item, slot) with N the
+// unit's slot count (the item releases the slot), then release the
+// activations.  Returns false on a timeout.
+template <typename ItemFn>
+__device__ bool consume(const Smem& m, const Range& rg, int ipe, const ThinUnit* units, int c,
+                        int nc, ItemFn item) {
+    const int lane = threadIdx.x & 31;
+    for (int u = rg.u_first; u <= rg.u_last; ++u) {
+        if (!warp_wait(m.act_full(), (uint32_t)((u - rg.u_first) & 1))) return false;
+        const int s0 = max(u * ipe, rg.beg) - rg.beg;
+        const int s1 = min((u + 1) * ipe, rg.beg + rg.cnt) - rg.beg;
+        const int first = s0 + ((c - s0 % nc) + nc) % nc;
+        bool ok = true;
+        with_slots(units[u].n, [&]<int N>() {
+            int slot = first % m.slots, round = first / m.slots;
+            for (int seq = first; seq < s1; seq += nc) {
+                if (round > 0 && !warp_wait(m.empty(slot), (uint32_t)((round - 1) & 1))) {
+                    ok = false;
+                    return;
+                }
+                if (!warp_wait(m.full(slot), (uint32_t)(round & 1))) {
+                    ok = false;
+                    return;
+                }
+                item.template operator()<N>(rg.beg + seq, slot);
+                slot += nc;            // nc < slots: at most one wrap
+                if (slot >= m.slots) {
+                    slot -= m.slots;
+                    ++round;
+                }
+            }
+        });
+        if (!ok) return false;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(m.act_free());
     }
+    return true;
+}
+
+// ---- compute ------------------------------------------------------------------
+//
+// Rows are read lane-interleaved: vector v of a row = lane + 32 * j.  `vec`
+// is the row length in 16-byte vectors (a multiple of 32); activation row t
+// starts at act + t * vec * 16.
+
+// Gate and up dot products; weight vectors come from wg_at(j) / wu_at(j)
+// (registers or shared memory).
+template <int N, int VPL, typename WG, typename WU>
+__device__ __forceinline__ void gate_up_dots(WG wg_at, WU wu_at, uint32_t act, int vec, int iters,
+                                             float (&g)[N], float (&u)[N]) {
+    constexpr int P = Chains<N>::P;
+    const int lane = threadIdx.x & 31;
+    float ga[N][P], ua[N][P];
+#pragma unroll
+    for (int t = 0; t < N; ++t)
+#pragma unroll
+        for (int p = 0; p < P; ++p) ga[t][p] = ua[t][p] = 0.f;
+#pragma unroll(VPL > 0 ? VPL : 2)
+    for (int j = 0; j < (VPL > 0 ? VPL : iters); ++j) {
+        const Bf16x8 wg(wg_at(j)), wu(wu_at(j));
+#pragma unroll
+        for (int t = 0; t < N; ++t) {
+            const Bf16x8 xa(lds128(act + (uint32_t)((t * vec + lane + 32 * j) * 16)));
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                fma_bf16(ga[t][q % P], wg.h[q], xa.h[q]);
+                fma_bf16(ua[t][q % P], wu.h[q], xa.h[q]);
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < N; ++t) {
+        g[t] = warp_sum(sum_chains<P>(ga[t]));
+        u[t] = warp_sum(sum_chains<P>(ua[t]));
+    }
+}
+
+template <int N, int VPL, typename W>
+__device__ __forceinline__ void down_dots(W w_at, uint32_t act, int vec, int iters,
+                                          float (&a)[N]) {
+    constexpr int P = Chains<N>::P;
+    const int lane = threadIdx.x & 31;
+    float acc[N][P];
+#pragma unroll
+    for (int t = 0; t < N; ++t)
+#pragma unroll
+        for (int p = 0; p < P; ++p) acc[t][p] = 0.f;
+#pragma unroll(VPL > 0 ? VPL : 2)
+    for (int j = 0; j < (VPL > 0 ? VPL : iters); ++j) {
+        const Bf16x8 fw(w_at(j));
+#pragma unroll
+        for (int t = 0; t < N; ++t) {
+            const Bf16x8 xa(lds128(act + (uint32_t)((t * vec + lane + 32 * j) * 16)));
+#pragma unroll
+            for (int q = 0; q < 8; ++q) fma_bf16(acc[t][q % P], fw.h[q], xa.h[q]);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < N; ++t) a[t] = warp_sum(sum_chains<P>(acc[t]));
+}
+
+template <int N>
+__device__ __forceinline__ void store_h(const float (&g)[N], const float (&u)[N],
+                                        __nv_bfloat16* hcol, int64_t ldh) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int t = 0; t < N; ++t)
+        if (lane == t) hcol[t * ldh] = __float2bfloat16_rn(silu_mul(g[t], u[t]));
+}
+
+template <int N>
+__device__ __forceinline__ void store_y(const float (&a)[N], __nv_bfloat16* ycol, int64_t ldy) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int t = 0; t < N; ++t)
+        if (lane == t) ycol[t * ldy] = __float2bfloat16_rn(a[t]);
+}
+
+// One gate/up slot: R rows of gate then R rows of up, rows of vec vectors.
+// VPL > 0 (= vec / 32, R = 16 / VPL): the lane's share is copied to
+// registers and the slot released before computing (N <= kRegSlots).
+template <int N, int VPL>
+__device__ __forceinline__ void gate_up_slot(const Smem& m, int slot, int R, int vec,
+                                             __nv_bfloat16* hcol, int64_t ldh) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t sg = m.buf(slot);
+    const uint32_t su = sg + (uint32_t)(R * vec * 16);
+    if constexpr (VPL > 0 && N <= kRegSlots) {
+        constexpr int RR = 16 / VPL;
+        uint4 wg[RR * VPL], wu[RR * VPL];
+#pragma unroll
+        for (int i = 0; i < RR * VPL; ++i) {
+            wg[i] = lds128(sg + (uint32_t)((i * 32 + lane) * 16));
+            wu[i] = lds128(su + (uint32_t)((i * 32 + lane) * 16));
+        }
+        release_slot(m, slot);
+#pragma unroll
+        for (int r = 0; r < RR; ++r) {
+            float g[N], u[N];
+            gate_up_dots<N, VPL>([&](int j) { return wg[r * VPL + j]; },
+                                 [&](int j) { return wu[r * VPL + j]; }, m.act, vec, VPL, g, u);
+            store_h<N>(g, u, hcol + r, ldh);
+        }
+    } else {
+        const int iters = vec >> 5;
+        for (int r = 0; r < R; ++r) {
+            const uint32_t rg = sg + (uint32_t)(r * vec * 16), ru = su + (uint32_t)(r * vec * 16);
+            float g[N], u[N];
+            gate_up_dots<N, 0>([&](int j) { return lds128(rg + (uint32_t)((lane + 32 * j) * 16)); },
+                               [&](int j) { return lds128(ru + (uint32_t)((lane + 32 * j) * 16)); },
+                               m.act, vec, iters, g, u);
+            store_h<N>(g, u, hcol + r, ldh);
+        }
+        release_slot(m, slot);
+    }
+}
+
+// One down slot: R rows of W_down of vec vectors.  VPL > 0 (= vec / 32,
+// R = 32 / VPL): register-cached as above.
+template <int N, int VPL>
+__device__ __forceinline__ void down_slot(const Smem& m, int slot, int R, int vec,
+                                          __nv_bfloat16* ycol, int64_t ldy) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t sw = m.buf(slot);
+    if constexpr (VPL > 0 && N <= kRegSlots) {
+        constexpr int RR = 32 / VPL;
+        uint4 w[RR * VPL];
+#pragma unroll
+        for (int i = 0; i < RR * VPL; ++i) w[i] = lds128(sw + (uint32_t)((i * 32 + lane) * 16));
+        release_slot(m, slot);
+#pragma unroll
+        for (int r = 0; r < RR; ++r) {
+            float a[N];
+            down_dots<N, VPL>([&](int j) { return w[r * VPL + j]; }, m.act, vec, VPL, a);
+            store_y<N>(a, ycol + r, ldy);
+        }
+    } else {
+        const int iters = vec >> 5;
+        for (int r = 0; r < R; ++r) {
+            const uint32_t rw = sw + (uint32_t)(r * vec * 16);
+            float a[N];
+            down_dots<N, 0>([&](int j) { return lds128(rw + (uint32_t)((lane + 32 * j) * 16)); },
+                            m.act, vec, iters, a);
+            store_y<N>(a, ycol + r, ldy);
+        }
+        release_slot(m, slot);
+    }
+}
+
+// ---- kernels -------------------------------------------------------------------
+
+// VPL = H / 256 when a 16 KB slot holds 16 / VPL whole rows each of gate and
+// up (H = 256 ... 4096): register-cached path for units of <= 4 slots; 0: any
+// H, rows read from shared memory.
+template <int VPL>
+__global__ void __launch_bounds__(kThreads, 1)
+thin_gate_up_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ perm,
+                    int k, int H, int I, int R, const __nv_bfloat16* __restrict__ Wg,
+                    const __nv_bfloat16* __restrict__ Wu, const ThinUnit* __restrict__ units,
+                    WsHeader* hdr, __nv_bfloat16* __restrict__ h, int stage_bytes, int slots,
+                    int act_bytes) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int kProducers = 2;   // warp 0 issues the gate rows, warp 1 the up rows
+    const int nc = (blockDim.x >> 5) - kProducers;
+    const Smem m = smem_setup(smem, stage_bytes, slots, act_bytes, kProducers, nc);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int vec = H / 8;
+    const int ipe = I / R;
+    const Range rg = cta_range(units, hdr, ipe);
+    const uint32_t half = (uint32_t)R * H * 2;
+    const uint32_t xrow = (uint32_t)H * 2;
+
+    if (warp < kProducers) {
+        if (lane == 0) {
+            const uint64_t policy = policy_evict_first();
+            const __nv_bfloat16* W = warp == 0 ? Wg : Wu;
+            const uint32_t part = warp == 0 ? 0u : half;
+            const bool ok = produce(
+                m, rg, warp == 0,
+                [&](int it, uint32_t dst, uint32_t bar) {
+                    const ThinUnit un = units[it / ipe];
+                    const size_t off = ((size_t)un.expert * I + (size_t)(it % ipe) * R) * H;
+                    mbar_expect_tx(bar, half);
+                    bulk_g2s_evict_first(dst + part, W + off, half, bar, policy);
+                },
+                [&](int u, uint32_t dst, uint32_t bar) {
+                    const ThinUnit un = units[u];
+                    mbar_expect_tx(bar, (uint32_t)un.n * xrow);
+                    for (int t = 0; t < un.n; ++t)
+                        bulk_g2s(dst + t * xrow, x + (size_t)(perm[un.row0 + t] / k) * H, xrow, bar);
+                });
+            if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
+        }
+        return;
+    }
+
+    const bool ok = consume(m, rg, ipe, units, warp - kProducers, nc, [&]<int N>(int it, int slot) {
+        const ThinUnit un = units[it / ipe];
+        __nv_bfloat16* hcol = h + (int64_t)un.row0 * I + (it % ipe) * R;
+        gate_up_slot<N, VPL>(m, slot, R, vec, hcol, I);
+    });
+    if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
+}
+
+// VPL = I / 256 when a 16 KB slot holds 32 / VPL whole rows of W_down
+// (I = 256 ... 8192): register-cached path for units of <= 4 slots; 0: any I.
+template <int VPL>
+__global__ void __launch_bounds__(kThreads, 1)
+thin_down_kernel(const __nv_bfloat16* __restrict__ h, int H, int I, int R,
+                 const __nv_bfloat16* __restrict__ Wd, const ThinUnit* __restrict__ units,
+                 WsHeader* hdr, __nv_bfloat16* __restrict__ y, int stage_bytes, int slots,
+                 int act_bytes) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int kProducers = 1;
+    const int nc = (blockDim.x >> 5) - kProducers;
+    const Smem m = smem_setup(smem, stage_bytes, slots, act_bytes, kProducers, nc);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int vec = I / 8;
+    const int ipe = H / R;
+    const Range rg = cta_range(units, hdr, ipe);
+    const uint32_t bytes = (uint32_t)R * I * 2;
+    const uint32_t hrow = (uint32_t)I * 2;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t policy = policy_evict_first();
+            const bool ok = produce(
+                m, rg, true,
+                [&](int it, uint32_t dst, uint32_t bar) {
+                    const ThinUnit un = units[it / ipe];
+                    mbar_expect_tx(bar, bytes);
+                    bulk_g2s_evict_first(
+                        dst, Wd + ((size_t)un.expert * H + (size_t)(it % ipe) * R) * I, bytes,
+                        bar, policy);
+                },
+                [&](int u, uint32_t dst, uint32_t bar) {
+                    const ThinUnit un = units[u];
+                    // the unit's h rows are consecutive sorted positions
+                    mbar_expect_tx(bar, (uint32_t)un.n * hrow);
+                    bulk_g2s(dst, h + (size_t)un.row0 * I, (uint32_t)un.n * hrow, bar);
+                });
+            if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
+        }
+        return;
+    }
+
+    const bool ok = consume(m, rg, ipe, units, warp - kProducers, nc, [&]<int N>(int it, int slot) {
+        const ThinUnit un = units[it / ipe];
+        __nv_bfloat16* ycol = y + (int64_t)un.row0 * H + (it % ipe) * R;
+        down_slot<N, VPL>(m, slot, R, vec, ycol, H);
+    });
+    if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
+}
+
+// Rows per item so that a weight slot holds at most kStageTarget bytes (at
+// least one row); a power of two, so it divides I and H (multiples of 256).
+int rows_per_item(int row_bytes) {
+    int r = 1;
+    while (2 * r * row_bytes <= kStageTarget && r < 256) r *= 2;
+    return r;
+}
+
+struct Geometry {
+    int R, stage, slots, act, smem;
+};
+
+// act_tokens: most slots any unit can hold here (the activation buffer size).
+Geometry geometry(int row_bytes, int act_row_bytes, int act_tokens) {
+    Geometry g;
+    g.R = rows_per_item(row_bytes);
+    g.stage = g.R * row_bytes;
+    g.act = act_tokens * act_row_bytes;
+    g.slots = (kSmemBudget - g.act) / g.stage;
+    if (g.slots > kMaxSlots) g.slots = kMaxSlots;
+    if (g.slots < 2) g.slots = 2;
+    g.smem = g.slots * g.stage + g.act + 8 * (2 * kMaxSlots + 2);
+    return g;
+}
+
+// Producers + consumers, with fewer consumers than slots (slot protocol).
+int threads_for(const Geometry& g, int producers) {
+    int consumers = kWarps - producers;
+    if (consumers > g.slots - 1) consumers = g.slots - 1;
+    if (consumers < 1) consumers = 1;
+    return 32 * (producers + consumers);
+}
+
+// Raises a kernel's dynamic shared-memory limit once per device (the launch
+// path then makes no extra runtime calls).
+template <typename K>
+cudaError_t ensure_smem(K kernel, int (&done)[64]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBudget + 1024);
+    if (e == cudaSuccess) done[dev] = 1;
+    return e;
+}
+
+template <int V>
+cudaError_t launch_gu(const __nv_bfloat16* x, const int32_t* perm, int k, int H, int I,
+                      const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, const Plan& plan,
+                      const Geometry& g, __nv_bfloat16* h, int num_sms, cudaStream_t s) {
+    static int done[64];
+    cudaError_t e = ensure_smem(thin_gate_up_kernel<V>, done);
+    if (e != cudaSuccess) return e;
+    thin_gate_up_kernel<V><<<num_sms, threads_for(g, 2), g.smem, s>>>(
+        x, perm, k, H, I, g.R, Wg, Wu, plan.units, plan.hdr, h, g.stage, g.slots, g.act);
+    return cudaGetLastError();
+}
+
+template <int V>
+cudaError_t launch_d(const __nv_bfloat16* h, int H, int I, const __nv_bfloat16* Wd,
+                     const Plan& plan, const Geometry& g, __nv_bfloat16* y, int num_sms,
+                     cudaStream_t s) {
+    static int done[64];
+    cudaError_t e = ensure_smem(thin_down_kernel<V>, done);
+    if (e != cudaSuccess) return e;
+    thin_down_kernel<V><<<num_sms, threads_for(g, 1), g.smem, s>>>(
+        h, H, I, g.R, Wd, plan.units, plan.hdr, y, g.stage, g.slots, g.act);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_thin_gate_up(const __nv_bfloat16* x, const int32_t* perm,
-                                const int32_t* offsets, const int32_t* counts,
-                                int k, int H, int I, const __nv_bfloat16* Wg,
-                                const __nv_bfloat16* Wu, const Plan& plan,
-                                __nv_bfloat16* h, int num_sms, cudaStream_t s) {
-    thin_gate_up_kernel<<<num_sms * 4, 32 * kWarpsPerBlock, 0, s>>>(
-        reinterpret_cast<const uint4*>(x), perm, offsets, counts, k, H, I,
-        reinterpret_cast<const uint4*>(Wg), reinterpret_cast<const uint4*>(Wu),
-        plan.thin, plan.hdr, h);
-    return cudaGetLastError();
+int thin_unit_tokens(int H, int I) {
+    const int row = 2 * (H > I ? H : I);
+    int nu = kActBudget / row;
+    if (nu > kMaxUnitTokens) nu = kMaxUnitTokens;
+    return nu < 1 ? 1 : nu;
 }
 
-cudaError_t launch_thin_down(const __nv_bfloat16* h, const int32_t* offsets,
-                             const int32_t* counts, int H, int I,
-                             const __nv_bfloat16* Wd, const Plan& plan,
-                             __nv_bfloat16* y_sorted, int num_sms,
-                             cudaStream_t s) {
-    thin_down_kernel<<<num_sms * 4, 32 * kWarpsPerBlock, 0, s>>>(
-        reinterpret_cast<const uint4*>(h), offsets, counts, H, I,
-        reinterpret_cast<const uint4*>(Wd), plan.thin, plan.hdr, y_sorted);
-    return cudaGetLastError();
+cudaError_t launch_thin_gate_up(const __nv_bfloat16* x, const int32_t* perm, int k, int H,
+                                int I, const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
+                                const Plan& plan, int64_t max_slots, __nv_bfloat16* h,
+                                int num_sms, cudaStream_t s) {
+    const int act_tokens =
+        (int)std::min<int64_t>(plan.unit_tokens, std::max<int64_t>(max_slots, 1));
+    const Geometry g = geometry(2 * H * 2, H * 2, act_tokens);
+    switch (g.stage == kStageTarget ? H : 0) {
+        case 256: return launch_gu<1>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s);
+        case 512: return launch_gu<2>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s);
+        case 1024: return launch_gu<4>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s);
+        case 2048: return launch_gu<8>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s);
+        case 4096: return launch_gu<16>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s);
+        default: return launch_gu<0>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s);
+    }
+}
+
+cudaError_t launch_thin_down(const __nv_bfloat16* h, int H, int I, const __nv_bfloat16* Wd,
+                             const Plan& plan, int64_t max_slots, __nv_bfloat16* y_sorted,
+                             int num_sms, cudaStream_t s) {
+    const int act_tokens =
+        (int)std::min<int64_t>(plan.unit_tokens, std::max<int64_t>(max_slots, 1));
+    const Geometry g = geometry(I * 2, I * 2, act_tokens);
+    switch (g.stage == kStageTarget ? I : 0) {
+        case 256: return launch_d<1>(h, H, I, Wd, plan, g, y_sorted, num_sms, s);
+        case 512: return launch_d<2>(h, H, I, Wd, plan, g, y_sorted, num_sms, s);
+        case 1024: return launch_d<4>(h, H, I, Wd, plan, g, y_sorted, num_sms, s);
+        case 2048: return launch_d<8>(h, H, I, Wd, plan, g, y_sorted, num_sms, s);
+        case 4096: return launch_d<16>(h, H, I, Wd, plan, g, y_sorted, num_sms, s);
+        case 8192: return launch_d<32>(h, H, I, Wd, plan, g, y_sorted, num_sms, s);
+        default: return launch_d<0>(h, H, I, Wd, plan, g, y_sorted, num_sms, s);
+    }
 }
 
 }  // namespace moe

@@ -68,6 +68,15 @@ def test_bad_shapes_rejected(moe, bad):
     assert lib.moe_last_error()
 
 
+def test_hidden_size_limit(moe):
+    lib = moe.binding.raw_lib()
+    shape = moe.binding.MoeShape(16, 16, 2, 16640, 256, 32)
+    assert lib.moe_workspace_size(ctypes.byref(shape)) == 0
+    st = lib.moe_forward(ctypes.byref(shape), None, None, None, None, None, None, None, None,
+                         None, 0, None)
+    assert st == 2
+
+
 def test_route_argument_errors(moe):
     lib = moe.binding.raw_lib()
     assert lib.moe_route(None, 4, 3, 4, None, None, None) == 1       # k > E

@@ -264,3 +264,25 @@ def test_decode_sweep_four_layers(moe):
             assert np.array_equal(idx.cpu().numpy(), oracle.route(inp["logits"].numpy(), s.k)[0])
     del layers
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("T,E,k,H,I", [(40, 8, 2, 768, 512), (20, 4, 4, 256, 768),
+                                       (70, 6, 3, 1280, 256), (33, 33, 1, 2048, 1024)])
+@pytest.mark.parametrize("thr", [0, 33])
+def test_forward_odd_shapes(moe, T, E, k, H, I, thr):
+    """Hidden sizes that are not powers of two, both expert paths."""
+    s = synth.Shape(T=T, E=E, k=k, H=H, I=I)
+    _full_check(moe, s, thr, synth.make_layer(s, seed=T, zipf_s=synth.ZIPF_S))
+
+
+def test_thin_units_split_at_full_width(moe):
+    """Full-width experts (H=4096, I=2048) with 1..32 slots on the weight-
+    streaming path (threshold 33): experts with more slots than one unit
+    holds are split into several units, each streaming the weights again."""
+    counts = [1, 12, 13, 24, 25, 31, 32, 2]
+    E = len(counts)
+    lg = _assigned_logits(counts, E)
+    s = synth.Shape(T=lg.shape[0], E=E, k=1, H=4096, I=2048)
+    inp = synth.make_layer(s, seed=8)
+    inp["logits"] = lg
+    _full_check(moe, s, 33, inp)
