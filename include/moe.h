@@ -213,6 +213,42 @@ moe_status moe_forward_profiled(const moe_shape* shape, const float* logits,
  * launch sequence depends only on the shape), or -1 for an invalid shape. */
 int32_t moe_forward_launches(const moe_shape* shape);
 
+/* ---- expert offload: pinned host memory -> HBM staging slots ---------- */
+
+/* Expert weights kept in pinned host memory and streamed into a ring of
+ * device staging slots on a side copy stream, overlapped with compute, the
+ * copy engine running ahead into the next layers (dsv41-flash-offload wiki,
+ * overview: experts pinned in host RAM, copied into VRAM slots in batches on
+ * the copy engine, 8 staging slots, cross-layer DMA prefetch).  One slot holds
+ * one layer's whole expert set. */
+typedef struct moe_stager moe_stager;
+
+/* Bytes of one layer's expert set: W_gate | W_up | W_down, bf16, in that
+ * order and in the layouts moe_forward takes (0 for an invalid shape). */
+size_t moe_layer_weight_bytes(const moe_shape* shape);
+
+/* Creates a stager over caller-owned device memory `slots` (n_slots slots of
+ * slot_bytes each, 256-byte aligned, slot_bytes a multiple of 256).  The
+ * stager allocates no device memory; it owns two CUDA events per slot.  The
+ * slots must outlive the stager and every forward enqueued with it. */
+moe_status moe_stager_create(void* slots, int32_t n_slots, size_t slot_bytes,
+                             moe_stager** out);
+moe_status moe_stager_destroy(moe_stager* stager);
+
+/* Runs n_layers independent layers on the same activations x [T, H] (device):
+ * for layer l, host_weights[l] (pinned host memory, moe_layer_weight_bytes
+ * bytes, W_gate | W_up | W_down) is copied into slot l mod n_slots on `copy`
+ * once the compute that last used that slot has finished, and moe_forward
+ * runs on `compute` once the copy has landed, with logits[l] [T, E] and
+ * out[l] [T, H] (device).  All copies are enqueued up front, so the copy
+ * engine works up to n_slots layers ahead.  `copy` must differ from
+ * `compute`; ws as for moe_forward.  Asynchronous; errors as moe_forward. */
+moe_status moe_forward_offload(moe_stager* stager, const moe_shape* shape, int32_t n_layers,
+                               const float* const* logits, const moe_bf16* x,
+                               const void* const* host_weights, moe_bf16* const* out,
+                               void* ws, size_t ws_bytes, moe_stream_t compute,
+                               moe_stream_t copy);
+
 /* ---- workspace status ---------------------------------------------- */
 
 /* Clears the status word of a fresh workspace (asynchronous on stream). */

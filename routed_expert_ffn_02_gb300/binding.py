@@ -34,7 +34,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTED = ("moe_route", "moe_permute_workspace_size", "moe_permute", "moe_permute_noalloc",
             "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
             "moe_workspace_size", "moe_forward", "moe_forward_profiled",
-            "moe_forward_launches", "moe_workspace_init",
+            "moe_forward_launches", "moe_layer_weight_bytes", "moe_stager_create",
+            "moe_stager_destroy", "moe_forward_offload", "moe_workspace_init",
             "moe_workspace_status", "moe_last_error", "moe_version")
 
 
@@ -86,6 +87,11 @@ _sig = {
     "moe_forward_profiled": ([_SP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _sz, _P,
                               ctypes.POINTER(ctypes.c_void_p), _i32], _i32),
     "moe_forward_launches": ([_SP], _i32),
+    "moe_layer_weight_bytes": ([_SP], _sz),
+    "moe_stager_create": ([_P, _i32, _sz, ctypes.POINTER(_P)], _i32),
+    "moe_stager_destroy": ([_P], _i32),
+    "moe_forward_offload": ([_P, _SP, _i32, ctypes.POINTER(_P), _P, ctypes.POINTER(_P),
+                             ctypes.POINTER(_P), _P, _sz, _P, _P], _i32),
     "moe_workspace_init": ([_P, _sz, _P], _i32),
     "moe_workspace_status": ([_P, _P, _i32], _i32),
     "moe_last_error": ([], ctypes.c_char_p),
@@ -263,6 +269,66 @@ def moe_forward_profiled(shape: Shape, logits, x, W_gate, W_up, W_down, events, 
 def forward_launches(shape: Shape) -> int:
     """Kernels one moe_forward call launches for this shape."""
     return _lib.moe_forward_launches(ctypes.byref(shape.c()))
+
+
+def layer_weight_bytes(shape: Shape) -> int:
+    """Bytes of one layer's expert set (W_gate | W_up | W_down, bf16)."""
+    return _lib.moe_layer_weight_bytes(ctypes.byref(shape.c()))
+
+
+def pack_layer_weights(W_gate, W_up, W_down, pin: bool = True) -> torch.Tensor:
+    """One layer's experts as the contiguous W_gate | W_up | W_down block the
+    stager copies (pinned host memory by default)."""
+    flat = torch.cat([W_gate.reshape(-1), W_up.reshape(-1), W_down.reshape(-1)]).cpu()
+    return flat.pin_memory() if pin else flat
+
+
+class Stager:
+    """Ring of `n_slots` device staging slots (allocated here with torch, owned
+    by this object) plus the library's stager over them."""
+
+    def __init__(self, shape: Shape, n_slots: int, device=None):
+        device = device or torch.device("cuda", torch.cuda.current_device())
+        self.slot_bytes = (layer_weight_bytes(shape) + 255) // 256 * 256
+        self.n_slots = n_slots
+        self._mem = torch.empty(n_slots * self.slot_bytes + 256, dtype=torch.uint8, device=device)
+        off = (-self._mem.data_ptr()) % 256
+        self.slots = self._mem[off:off + n_slots * self.slot_bytes]
+        self._h = ctypes.c_void_p()
+        _check(_lib.moe_stager_create(ctypes.c_void_p(self.slots.data_ptr()), n_slots,
+                                      self.slot_bytes, ctypes.byref(self._h)), "moe_stager_create")
+
+    def close(self):
+        if self._h:
+            _lib.moe_stager_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def forward(self, shape: Shape, logits, x, host_weights, outs=None, ws: Workspace | None = None,
+                compute=None, copy=None):
+        """Runs len(host_weights) layers; logits[l] and outs[l] are device
+        tensors, host_weights[l] pinned host blocks from pack_layer_weights.
+        Returns the outputs."""
+        L = len(host_weights)
+        dev = x.device
+        outs = outs if outs is not None else [
+            torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+        ws = ws or Workspace(workspace_size(shape), dev, compute)
+        compute = compute if compute is not None else torch.cuda.current_stream()
+        copy = copy if copy is not None else torch.cuda.Stream(device=dev)
+        PA = ctypes.c_void_p * max(L, 1)
+        lg = PA(*[ctypes.c_void_p(t.data_ptr()) for t in logits])
+        hw = PA(*[ctypes.c_void_p(t.data_ptr()) for t in host_weights])
+        op = PA(*[ctypes.c_void_p(t.data_ptr()) for t in outs])
+        _check(_lib.moe_forward_offload(self._h, ctypes.byref(shape.c()), L, lg, _ptr(x), hw, op,
+                                        ws.ptr, ws.nbytes, ctypes.c_void_p(compute.cuda_stream),
+                                        ctypes.c_void_p(copy.cuda_stream)), "moe_forward_offload")
+        return outs
 
 
 def raw_lib():

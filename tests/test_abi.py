@@ -119,3 +119,15 @@ def test_product_path_does_not_import_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in src and "from oracle" not in src, f
                 assert "moe_oracle" not in src, f
+
+
+def test_stager_argument_errors(moe):
+    lib = moe.binding.raw_lib()
+    shape = moe.binding.MoeShape(16, 16, 2, 512, 256, 32)
+    assert lib.moe_layer_weight_bytes(ctypes.byref(shape)) == 3 * 16 * 512 * 256 * 2
+    h = ctypes.c_void_p()
+    assert lib.moe_stager_create(None, 2, 1 << 20, ctypes.byref(h)) == 1
+    assert lib.moe_stager_create(ctypes.c_void_p(0x10000), 0, 1 << 20, ctypes.byref(h)) == 1
+    assert lib.moe_stager_create(ctypes.c_void_p(0x10010), 2, 1 << 20, ctypes.byref(h)) == 1
+    assert lib.moe_forward_offload(None, ctypes.byref(shape), 1, None, None, None, None, None, 0,
+                                   None, None) == 1
