@@ -27,9 +27,9 @@
 //     released, then for the current round to land; with more slots than
 //     consumers this makes every parity wait unambiguous.
 //   * A consumer lane covers the 16-byte vectors lane, lane+32, ... of a row.
-//     With few slots (<= 4) it copies its share of the whole slot into
-//     registers and releases the slot at once, so the ring refills while it
-//     computes.  Products are mixed-precision FMAs (fma.rn.f32.bf16: bf16
+//     It copies its share of the whole slot into registers and releases the
+//     slot at once, so the ring refills while it computes (row lengths of
+//     256 ... 4096 elements; other lengths compute from shared memory).  Products are mixed-precision FMAs (fma.rn.f32.bf16: bf16
 //     operands straight from the staged data, fp32 accumulators, no
 //     conversions) spread over enough independent accumulators to cover the
 //     FMA latency; the warp finishes each row with shuffle reductions and
@@ -58,7 +58,19 @@ constexpr int kSmemBudget = 224 * 1024;
 constexpr int kActBudget = 96 * 1024;          // activation buffer
 constexpr int kStageTarget = 16384;            // bytes per weight slot
 constexpr int kMaxUnitTokens = 16;
-constexpr int kRegSlots = 4;                   // register-cached path up to this many slots
+// Register-cached path: a lane holds 32 vectors of a slot (128 registers) and
+// the row loop is unrolled over them, so it is taken for units of at most 4
+// slots (more would not fit the instruction cache).
+template <int VPL>
+struct RegSlots {
+    static constexpr int value = 4;
+};
+// Down slots hold 32 / VPL rows, computed together (accumulators per row and
+// slot): while that is at most 4 rows, else the shared-memory path.
+template <int VPL>
+struct DownRegSlots {
+    static constexpr int value = VPL >= 8 ? 4 : 0;
+};
 
 // ---- shared loads, mixed-precision FMA ---------------------------------------
 
@@ -414,14 +426,14 @@ __device__ __forceinline__ void store_y(const float (&a)[N], __nv_bfloat16* ycol
 
 // One gate/up slot: R rows of gate then R rows of up, rows of vec vectors.
 // VPL > 0 (= vec / 32, R = 16 / VPL): the lane's share is copied to
-// registers and the slot released before computing (N <= kRegSlots).
+// registers and the slot released before computing (N <= RegSlots).
 template <int N, int VPL>
 __device__ __forceinline__ void gate_up_slot(const Smem& m, int slot, int R, int vec,
                                              __nv_bfloat16* hcol, int64_t ldh) {
     const int lane = threadIdx.x & 31;
     const uint32_t sg = m.buf(slot);
     const uint32_t su = sg + (uint32_t)(R * vec * 16);
-    if constexpr (VPL > 0 && N <= kRegSlots) {
+    if constexpr (VPL > 0 && N <= RegSlots<VPL>::value) {
         constexpr int RR = 16 / VPL;
         uint4 wg[RR * VPL], wu[RR * VPL];
 #pragma unroll
@@ -451,24 +463,60 @@ __device__ __forceinline__ void gate_up_slot(const Smem& m, int slot, int R, int
     }
 }
 
+// All RR rows of a register-cached down slot at once: each activation vector
+// is loaded once and applied to every row (w[r * VPL + j] = row r, vector j).
+template <int N, int VPL, int RR>
+__device__ __forceinline__ void down_rows_regs(const uint4 (&w)[RR * VPL], uint32_t act, int vec,
+                                               float (&a)[RR][N]) {
+    constexpr int P = Chains<N * RR>::P;
+    const int lane = threadIdx.x & 31;
+    float acc[RR][N][P];
+#pragma unroll
+    for (int r = 0; r < RR; ++r)
+#pragma unroll
+        for (int t = 0; t < N; ++t)
+#pragma unroll
+            for (int p = 0; p < P; ++p) acc[r][t][p] = 0.f;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+#pragma unroll
+        for (int t = 0; t < N; ++t) {
+            const Bf16x8 xa(lds128(act + (uint32_t)((t * vec + lane + 32 * j) * 16)));
+#pragma unroll
+            for (int r = 0; r < RR; ++r) {
+                const Bf16x8 fw(w[r * VPL + j]);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) fma_bf16(acc[r][t][q % P], fw.h[q], xa.h[q]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < RR; ++r)
+#pragma unroll
+        for (int t = 0; t < N; ++t) a[r][t] = warp_sum(sum_chains<P>(acc[r][t]));
+}
+
 // One down slot: R rows of W_down of vec vectors.  VPL > 0 (= vec / 32,
-// R = 32 / VPL): register-cached as above.
+// R = 32 / VPL): the lane's share is copied to registers, the slot released,
+// and all rows computed together.
 template <int N, int VPL>
 __device__ __forceinline__ void down_slot(const Smem& m, int slot, int R, int vec,
                                           __nv_bfloat16* ycol, int64_t ldy) {
     const int lane = threadIdx.x & 31;
     const uint32_t sw = m.buf(slot);
-    if constexpr (VPL > 0 && N <= kRegSlots) {
+    if constexpr (VPL > 0 && N <= DownRegSlots<VPL>::value) {
         constexpr int RR = 32 / VPL;
         uint4 w[RR * VPL];
 #pragma unroll
         for (int i = 0; i < RR * VPL; ++i) w[i] = lds128(sw + (uint32_t)((i * 32 + lane) * 16));
         release_slot(m, slot);
+        float a[RR][N];
+        down_rows_regs<N, VPL, RR>(w, m.act, vec, a);
 #pragma unroll
         for (int r = 0; r < RR; ++r) {
-            float a[N];
-            down_dots<N, VPL>([&](int j) { return w[r * VPL + j]; }, m.act, vec, VPL, a);
-            store_y<N>(a, ycol + r, ldy);
+#pragma unroll
+            for (int t = 0; t < N; ++t)
+                if (lane == t) ycol[t * ldy + r] = __float2bfloat16_rn(a[r][t]);
         }
     } else {
         const int iters = vec >> 5;
@@ -539,7 +587,7 @@ thin_gate_up_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
 }
 
 // VPL = I / 256 when a 16 KB slot holds 32 / VPL whole rows of W_down
-// (I = 256 ... 8192): register-cached path for units of <= 4 slots; 0: any I.
+// (I = 256 ... 8192): register-cached path; 0: any I.
 template <int VPL>
 __global__ void __launch_bounds__(kThreads, 1)
 thin_down_kernel(const __nv_bfloat16* __restrict__ h, int H, int I, int R,
