@@ -4,8 +4,9 @@
 Headline workload: one MoE layer over a 16,384-token prefill chunk (384
 experts, top-8, H=4096, I=2048, bf16, Zipf(1.1)-skewed router logits, fat
 threshold 32).  A step is one moe_forward: route, route lists, both expert
-paths and the combine.  Decode batches 1 and 4 on the same layer are
-reported beside it.
+paths and the combine.  Reported beside it: decode batches 1 and 4 on the
+same layer, the decode batch sweep 1..24 over 4 resident layers, and (with
+--offload) the 12-layer prefill streamed from pinned host memory.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 
@@ -358,6 +359,67 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------- decode sweep
+
+def run_sweep(moe, dev, base_weights, peaks, reps=40, warmup=5, n_layers=4, n_sets=4):
+    """Decode batches 1..24 through 4 resident MoE layers (384 experts,
+    H=4096, I=2048, bf16; 77 GB of weights so L2 cannot hold them).  A step is
+    one batch through all 4 layers, replayed from a CUDA graph; n_sets logit
+    sets rotate so the touched experts change from step to step."""
+    E, H, I, k = PREFILL.E, PREFILL.H, PREFILL.I, PREFILL.k
+    layers = [base_weights] + [synth.make_weights(E, H, I, seed=0, layer=l, device=dev)
+                               for l in range(1, n_layers)]
+    expert_bytes = 3 * H * I * 2
+    out = {}
+    for B in synth.DECODE_SWEEP_BATCHES:
+        shape = moe.Shape(B, E, k, H, I, FAT_THRESHOLD)
+        ws = moe.Workspace(moe.workspace_size(shape), dev)
+        x = synth.make_x(B, H, seed=0).to(dev)
+        lg = [[synth.make_logits(B, E, seed=0, layer=l, rep=r, zipf_s=synth.ZIPF_S).to(dev)
+               for l in range(n_layers)] for r in range(n_sets)]
+        outs = [torch.empty((B, H), dtype=torch.bfloat16, device=dev) for _ in range(n_layers)]
+        touched = []
+        for r in range(n_sets):
+            for l in range(n_layers):
+                idx, _ = moe.moe_route(lg[r][l], k)
+                touched.append(int(torch.unique(idx).numel()))
+        stream = torch.cuda.Stream()
+        graphs = []
+        with torch.cuda.stream(stream):
+            for r in range(n_sets):
+                for l in range(n_layers):
+                    moe.moe_forward(shape, lg[r][l], x, *layers[l], out=outs[l], ws=ws)
+            torch.cuda.synchronize()
+            for r in range(n_sets):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for l in range(n_layers):
+                        moe.moe_forward(shape, lg[r][l], x, *layers[l], out=outs[l], ws=ws)
+                graphs.append(g)
+        for i in range(warmup):
+            graphs[i % n_sets].replay()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record()
+        for i in range(reps):
+            graphs[i % n_sets].replay()
+        t1.record()
+        torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1) / reps
+        bytes_step = sum(touched) / n_sets * expert_bytes
+        out[f"B{B}"] = {
+            "tokens_per_s": round(B / (ms * 1e-3), 1),
+            "us_per_step": round(1e3 * ms, 2),
+            "touched_experts_per_layer": round(sum(touched) / len(touched), 2),
+            "frac_of_hbm_roofline": round(bytes_step / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+        }
+        del graphs, ws
+    del layers[1:]
+    torch.cuda.empty_cache()
+    return out
+
+
 # --------------------------------------------------------------- offload
 
 def run_offload(args, moe, dev, n_layers=12, n_slots=8):
@@ -534,6 +596,9 @@ def run_gpu(args):
                          f"({n * shape.k} token-expert pairs, {n_exp} experts), "
                          f"single-threaded fp64, {dt:.1f} s"}
 
+    sweep = None
+    if not args.no_sweep:
+        sweep = run_sweep(moe, dev, (layer.Wg, layer.Wu, layer.Wd), peaks)
     offload = run_offload(args, moe, dev) if args.offload else None
 
     launches = moe.forward_launches(shape) * args.steps
@@ -564,6 +629,7 @@ def run_gpu(args):
             "gpu_launches": launches,
             "clocks": clk.summary(),
             "decode": decode,
+            "decode_sweep_4_layers": sweep,
             "offload": offload,
             "peaks": peaks,
         }
@@ -584,6 +650,8 @@ def main():
                     help="override T of the layer (small cases for profiling)")
     ap.add_argument("--experts", type=int, default=None,
                     help="override E of the layer (small cases for profiling)")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the decode batch sweep over 4 resident layers")
     ap.add_argument("--offload", action="store_true",
                     help="also run the offload prefill (58 GB of experts in pinned host memory)")
     ap.add_argument("--traffic", type=float, default=None,

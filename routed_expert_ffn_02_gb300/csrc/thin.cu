@@ -281,9 +281,16 @@ __device__ __forceinline__ void release_slot(const Smem& m, int slot) {
     if ((threadIdx.x & 31) == 0) mbar_arrive(m.empty(slot));
 }
 
-// Calls f.template operator()<N>() for the runtime slot count n in [1, 16].
-template <typename F>
+// Calls f.template operator()<N>() for the runtime slot count n in [1, 16];
+// with kExact < 16, counts above kExact all go to N = kExact + 1.
+template <int kExact = 16, typename F>
 __device__ __forceinline__ void with_slots(int n, F&& f) {
+    if constexpr (kExact < 16) {
+        if (n > kExact) {
+            f.template operator()<kExact + 1>();
+            return;
+        }
+    }
     switch (n) {
         case 1: f.template operator()<1>(); break;
         case 2: f.template operator()<2>(); break;
@@ -309,7 +316,7 @@ __device__ __forceinline__ void with_slots(int n, F&& f) {
 // for the slot and run item.template operator()<N>(item, slot) with N the
 // unit's slot count (the item releases the slot), then release the
 // activations.  Returns false on a timeout.
-template <typename ItemFn>
+template <int kExact, typename ItemFn>
 __device__ bool consume(const Smem& m, const Range& rg, int ipe, const ThinUnit* units, int c,
                         int nc, ItemFn item) {
     const int lane = threadIdx.x & 31;
@@ -319,7 +326,7 @@ __device__ bool consume(const Smem& m, const Range& rg, int ipe, const ThinUnit*
         const int s1 = min((u + 1) * ipe, rg.beg + rg.cnt) - rg.beg;
         const int first = s0 + ((c - s0 % nc) + nc) % nc;
         bool ok = true;
-        with_slots(units[u].n, [&]<int N>() {
+        with_slots<kExact>(units[u].n, [&]<int N>() {
             int slot = first % m.slots, round = first / m.slots;
             for (int seq = first; seq < s1; seq += nc) {
                 if (round > 0 && !warp_wait(m.empty(slot), (uint32_t)((round - 1) & 1))) {
@@ -424,11 +431,58 @@ __device__ __forceinline__ void store_y(const float (&a)[N], __nv_bfloat16* ycol
         if (lane == t) ycol[t * ldy] = __float2bfloat16_rn(a[t]);
 }
 
+// Register-cached down slots of units with more than 4 slots: runtime loop
+// over groups of 4 slots, so one compiled body (4 slots x RR rows x VPL
+// vectors) serves every count and the weights stay in registers across groups
+// (measured faster than computing from shared memory for down; for gate/up,
+// whose slot is one long row pair, it was slower).  The last group may read
+// activation rows past n (the buffer is padded to a multiple of 4 rows); their
+// results are not stored.
+template <int VPL, int RR>
+__device__ __forceinline__ void down_groups_regs(const uint4 (&w)[RR * VPL], uint32_t act,
+                                                 int vec, int n, __nv_bfloat16* ycol,
+                                                 int64_t ldy) {
+    constexpr int G = 4;
+    constexpr int P = Chains<G * RR>::P;
+    const int lane = threadIdx.x & 31;
+#pragma unroll 1
+    for (int t0 = 0; t0 < n; t0 += G) {
+        float acc[RR][G][P];
+#pragma unroll
+        for (int r = 0; r < RR; ++r)
+#pragma unroll
+            for (int t = 0; t < G; ++t)
+#pragma unroll
+                for (int p = 0; p < P; ++p) acc[r][t][p] = 0.f;
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+#pragma unroll
+            for (int t = 0; t < G; ++t) {
+                const Bf16x8 xa(lds128(act + (uint32_t)(((t0 + t) * vec + lane + 32 * j) * 16)));
+#pragma unroll
+                for (int r = 0; r < RR; ++r) {
+                    const Bf16x8 fw(w[r * VPL + j]);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) fma_bf16(acc[r][t][q % P], fw.h[q], xa.h[q]);
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RR; ++r)
+#pragma unroll
+            for (int t = 0; t < G; ++t) {
+                const float a = warp_sum(sum_chains<P>(acc[r][t]));
+                if (lane == t && t0 + t < n)
+                    ycol[(int64_t)(t0 + t) * ldy + r] = __float2bfloat16_rn(a);
+            }
+    }
+}
+
 // One gate/up slot: R rows of gate then R rows of up, rows of vec vectors.
 // VPL > 0 (= vec / 32, R = 16 / VPL): the lane's share is copied to
 // registers and the slot released before computing (N <= RegSlots).
 template <int N, int VPL>
-__device__ __forceinline__ void gate_up_slot(const Smem& m, int slot, int R, int vec,
+__device__ __forceinline__ void gate_up_slot(const Smem& m, int slot, int R, int vec, int n_slots,
                                              __nv_bfloat16* hcol, int64_t ldh) {
     const int lane = threadIdx.x & 31;
     const uint32_t sg = m.buf(slot);
@@ -500,23 +554,27 @@ __device__ __forceinline__ void down_rows_regs(const uint4 (&w)[RR * VPL], uint3
 // R = 32 / VPL): the lane's share is copied to registers, the slot released,
 // and all rows computed together.
 template <int N, int VPL>
-__device__ __forceinline__ void down_slot(const Smem& m, int slot, int R, int vec,
+__device__ __forceinline__ void down_slot(const Smem& m, int slot, int R, int vec, int n_slots,
                                           __nv_bfloat16* ycol, int64_t ldy) {
     const int lane = threadIdx.x & 31;
     const uint32_t sw = m.buf(slot);
-    if constexpr (VPL > 0 && N <= DownRegSlots<VPL>::value) {
+    if constexpr (VPL > 0 && DownRegSlots<VPL>::value > 0) {
         constexpr int RR = 32 / VPL;
         uint4 w[RR * VPL];
 #pragma unroll
         for (int i = 0; i < RR * VPL; ++i) w[i] = lds128(sw + (uint32_t)((i * 32 + lane) * 16));
         release_slot(m, slot);
-        float a[RR][N];
-        down_rows_regs<N, VPL, RR>(w, m.act, vec, a);
+        if constexpr (N <= DownRegSlots<VPL>::value) {
+            float a[RR][N];
+            down_rows_regs<N, VPL, RR>(w, m.act, vec, a);
 #pragma unroll
-        for (int r = 0; r < RR; ++r) {
+            for (int r = 0; r < RR; ++r) {
 #pragma unroll
-            for (int t = 0; t < N; ++t)
-                if (lane == t) ycol[t * ldy + r] = __float2bfloat16_rn(a[r][t]);
+                for (int t = 0; t < N; ++t)
+                    if (lane == t) ycol[t * ldy + r] = __float2bfloat16_rn(a[r][t]);
+            }
+        } else {
+            down_groups_regs<VPL, RR>(w, m.act, vec, n_slots, ycol, ldy);
         }
     } else {
         const int iters = vec >> 5;
@@ -578,10 +636,10 @@ thin_gate_up_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
         return;
     }
 
-    const bool ok = consume(m, rg, ipe, units, warp - kProducers, nc, [&]<int N>(int it, int slot) {
+    const bool ok = consume<16>(m, rg, ipe, units, warp - kProducers, nc, [&]<int N>(int it, int slot) {
         const ThinUnit un = units[it / ipe];
         __nv_bfloat16* hcol = h + (int64_t)un.row0 * I + (it % ipe) * R;
-        gate_up_slot<N, VPL>(m, slot, R, vec, hcol, I);
+        gate_up_slot<N, VPL>(m, slot, R, vec, un.n, hcol, I);
     });
     if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
 }
@@ -628,10 +686,11 @@ thin_down_kernel(const __nv_bfloat16* __restrict__ h, int H, int I, int R,
         return;
     }
 
-    const bool ok = consume(m, rg, ipe, units, warp - kProducers, nc, [&]<int N>(int it, int slot) {
+    constexpr int kExact = (VPL > 0 && DownRegSlots<VPL>::value > 0) ? DownRegSlots<VPL>::value : 16;
+    const bool ok = consume<kExact>(m, rg, ipe, units, warp - kProducers, nc, [&]<int N>(int it, int slot) {
         const ThinUnit un = units[it / ipe];
         __nv_bfloat16* ycol = y + (int64_t)un.row0 * H + (it % ipe) * R;
-        down_slot<N, VPL>(m, slot, R, vec, ycol, H);
+        down_slot<N, VPL>(m, slot, R, vec, un.n, ycol, H);
     });
     if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
 }
@@ -653,7 +712,7 @@ Geometry geometry(int row_bytes, int act_row_bytes, int act_tokens) {
     Geometry g;
     g.R = rows_per_item(row_bytes);
     g.stage = g.R * row_bytes;
-    g.act = act_tokens * act_row_bytes;
+    g.act = ((act_tokens + 3) / 4 * 4) * act_row_bytes;   // groups of 4 read whole groups
     g.slots = (kSmemBudget - g.act) / g.stage;
     if (g.slots > kMaxSlots) g.slots = kMaxSlots;
     if (g.slots < 2) g.slots = 2;
