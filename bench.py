@@ -361,7 +361,8 @@ def run_reference(args):
 
 # ----------------------------------------------------------- decode sweep
 
-def run_sweep(moe, dev, base_weights, peaks, reps=40, warmup=5, n_layers=4, n_sets=4):
+def run_sweep(moe, dev, base_weights, peaks, thin_mma_min=0, reps=40, warmup=5, n_layers=4,
+              n_sets=4):
     """Decode batches 1..24 through 4 resident MoE layers (384 experts,
     H=4096, I=2048, bf16; 77 GB of weights so L2 cannot hold them).  A step is
     one batch through all 4 layers, replayed from a CUDA graph; n_sets logit
@@ -372,7 +373,7 @@ def run_sweep(moe, dev, base_weights, peaks, reps=40, warmup=5, n_layers=4, n_se
     expert_bytes = 3 * H * I * 2
     out = {}
     for B in synth.DECODE_SWEEP_BATCHES:
-        shape = moe.Shape(B, E, k, H, I, FAT_THRESHOLD)
+        shape = moe.Shape(B, E, k, H, I, FAT_THRESHOLD, thin_mma_min)
         ws = moe.Workspace(moe.workspace_size(shape), dev)
         x = synth.make_x(B, H, seed=0).to(dev)
         lg = [[synth.make_logits(B, E, seed=0, layer=l, rep=r, zipf_s=synth.ZIPF_S).to(dev)
@@ -428,7 +429,7 @@ def run_offload(args, moe, dev, n_layers=12, n_slots=8):
     stream while the layers run on a 16,384-token chunk.  A step is the whole
     chunk through all 12 layers."""
     s = synth.OFFLOAD
-    shape = moe.Shape(s.T, s.E, s.k, s.H, s.I, FAT_THRESHOLD)
+    shape = moe.Shape(s.T, s.E, s.k, s.H, s.I, FAT_THRESHOLD, args.thin_mma_min)
     host = []
     for l in range(n_layers):
         W = synth.make_weights(s.E, s.H, s.I, seed=0, layer=l, device=dev)
@@ -491,7 +492,7 @@ def run_gpu(args):
 
     T = args.tokens or PREFILL.T
     E = args.experts or PREFILL.E
-    shape = moe.Shape(T, E, PREFILL.k, PREFILL.H, PREFILL.I, FAT_THRESHOLD)
+    shape = moe.Shape(T, E, PREFILL.k, PREFILL.H, PREFILL.I, FAT_THRESHOLD, args.thin_mma_min)
     layer = Layer(moe, shape, dev, n_logit_sets=1)
     counts = layer.counts()
     work = stage_work(shape, counts)
@@ -563,7 +564,8 @@ def run_gpu(args):
     decode = {}
     if not args.no_decode:
         for B in (1, 4):
-            dshape = moe.Shape(B, PREFILL.E, PREFILL.k, PREFILL.H, PREFILL.I, FAT_THRESHOLD)
+            dshape = moe.Shape(B, PREFILL.E, PREFILL.k, PREFILL.H, PREFILL.I, FAT_THRESHOLD,
+                               args.thin_mma_min)
             dl = Layer(moe, dshape, dev, n_logit_sets=8, weights=(layer.Wg, layer.Wu, layer.Wd))
             dcounts = dl.counts()
             dwork = stage_work(dshape, dcounts)
@@ -598,7 +600,7 @@ def run_gpu(args):
 
     sweep = None
     if not args.no_sweep:
-        sweep = run_sweep(moe, dev, (layer.Wg, layer.Wu, layer.Wd), peaks)
+        sweep = run_sweep(moe, dev, (layer.Wg, layer.Wu, layer.Wd), peaks, args.thin_mma_min)
     offload = run_offload(args, moe, dev) if args.offload else None
 
     launches = moe.forward_launches(shape) * args.steps
@@ -617,6 +619,7 @@ def run_gpu(args):
                 "fat_experts": work["_info"]["fat_experts"],
                 "thin_experts": work["_info"]["thin_experts"],
                 "touched_experts": work["_info"]["touched"],
+                "thin_mma_min": shape.thin_mma_min or "default",
             },
             "roofline": roof,
             "layer_roofline": {"ideal_ms": round(layer_ideal_ms, 4),
@@ -654,6 +657,9 @@ def main():
                     help="skip the decode batch sweep over 4 resident layers")
     ap.add_argument("--offload", action="store_true",
                     help="also run the offload prefill (58 GB of experts in pinned host memory)")
+    ap.add_argument("--thin-mma-min", type=int, default=0,
+                    help="slots from which a thin expert streams on the tensor cores "
+                         "(0: library default; 33: CUDA cores only)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args()

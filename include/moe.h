@@ -79,6 +79,13 @@ typedef struct {
     int32_t H;              /* hidden size */
     int32_t I;              /* expert intermediate size */
     int32_t fat_threshold;  /* slots at which an expert takes the GEMM; 32 */
+    int32_t thin_mma_min;   /* slots at which a thin expert streams its weights
+                               through the tensor cores instead of CUDA-core
+                               FMAs, 0..33.  0 = by shape: 1 when
+                               min(E, T*k) * I/128 >= 384 (enough 128-row work
+                               items to fill the GPU), else 33.  Values above
+                               fat_threshold - 1 keep every thin expert on
+                               CUDA cores. */
 } moe_shape;
 
 /* ---- routing -------------------------------------------------------- */

@@ -42,7 +42,8 @@ EXPORTED = ("moe_route", "moe_permute_workspace_size", "moe_permute", "moe_permu
 class MoeShape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("H", ctypes.c_int32), ("I", ctypes.c_int32),
-                ("fat_threshold", ctypes.c_int32)]
+                ("fat_threshold", ctypes.c_int32),
+                ("thin_mma_min", ctypes.c_int32)]
 
 
 @dataclass(frozen=True)
@@ -53,9 +54,11 @@ class Shape:
     H: int
     I: int
     fat_threshold: int = 32
+    thin_mma_min: int = 0     # 0: library default; > fat_threshold - 1: CUDA cores only
 
     def c(self) -> MoeShape:
-        return MoeShape(self.T, self.E, self.k, self.H, self.I, self.fat_threshold)
+        return MoeShape(self.T, self.E, self.k, self.H, self.I, self.fat_threshold,
+                        self.thin_mma_min)
 
     @property
     def P(self) -> int:

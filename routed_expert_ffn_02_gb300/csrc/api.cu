@@ -99,7 +99,43 @@ moe_status check_shape(const moe_shape* sh) {
     if (sh->fat_threshold < 0 || sh->fat_threshold > kThinMaxTokens + 1)
         return fail(MOE_ERR_INVALID_ARG, "fat_threshold = %d outside [0, %d]", sh->fat_threshold,
                     kThinMaxTokens + 1);
+    if (sh->thin_mma_min < 0 || sh->thin_mma_min > kThinMaxTokens + 1)
+        return fail(MOE_ERR_INVALID_ARG, "thin_mma_min = %d outside [0, %d]", sh->thin_mma_min,
+                    kThinMaxTokens + 1);
     return MOE_OK;
+}
+
+// thin_mma_min == 0 picks the streaming kernel from the shape: the tensor-core
+// kernel's work items are 128-row weight blocks of whole experts, so it needs
+// enough thin experts to fill the GPU; below that the CUDA-core kernel, which
+// splits weight rows finely over all SMs, is faster.  At most min(E, T*k)
+// experts are touched.
+int thin_mma_min(const moe_shape* sh) {
+    if (sh->thin_mma_min > 0) return sh->thin_mma_min;
+    const int64_t touched = std::min<int64_t>(sh->E, (int64_t)sh->T * sh->k);
+    return touched * (sh->I / 128) >= kThinMmaAutoItems ? 1 : kThinMaxTokens + 1;
+}
+
+// Which expert kernels can have work, given an upper bound of any expert's
+// slot count (the planner decides on the device; a kernel with an empty
+// list returns at once, but one that cannot have work is not launched).
+struct ExpertKernels {
+    bool fat, units, mma;
+    bool gather() const { return fat || mma; }
+};
+ExpertKernels expert_kernels(const moe_shape* sh, int64_t fat_bound) {
+    const int thr = sh->fat_threshold, mm = thin_mma_min(sh);
+    ExpertKernels k;
+    k.fat = fat_bound >= std::max(thr, 1);
+    k.units = std::min(thr, mm) > 1;                     // counts in [1, min(thr, mm))
+    k.mma = thr > mm && fat_bound >= mm;                 // counts in [mm, thr)
+    return k;
+}
+
+Plan make_plan(const moe_shape* sh, FatTile* tiles, ThinUnit* units, FatTile* mma_tiles,
+               WsHeader* hdr) {
+    return Plan{tiles, units, mma_tiles, hdr, sh->fat_threshold,
+                thin_unit_tokens(sh->H, sh->I), thin_mma_min(sh)};
 }
 
 // Bump allocator over the caller's workspace (256-byte aligned regions).
@@ -122,6 +158,7 @@ struct FfnBufs {
     WsHeader* hdr;
     FatTile* tiles;
     ThinUnit* units;
+    FatTile* mma_tiles;
     __nv_bfloat16* x_sorted;
     __nv_bfloat16* h;
 };
@@ -132,6 +169,7 @@ struct FwdBufs {
     float* gates;
     FatTile* tiles;
     ThinUnit* units;
+    FatTile* mma_tiles;
     __nv_bfloat16* xy;   // x_sorted, later reused for y_sorted
     __nv_bfloat16* h;
 };
@@ -142,6 +180,7 @@ size_t carve_ffn(const moe_shape* sh, void* ws, FfnBufs* b) {
     b->hdr = c.take<WsHeader>(1);
     b->tiles = c.take<FatTile>((size_t)max_fat_tiles(P, sh->E));
     b->units = c.take<ThinUnit>((size_t)max_thin_units(sh->E, thin_unit_tokens(sh->H, sh->I)));
+    b->mma_tiles = c.take<FatTile>((size_t)sh->E);
     b->x_sorted = c.take<__nv_bfloat16>((size_t)(rows_alloc(P) * sh->H));
     b->h = c.take<__nv_bfloat16>((size_t)(rows_alloc(P) * sh->I));
     return align_up(c.off, 256);
@@ -160,6 +199,7 @@ size_t carve_fwd(const moe_shape* sh, void* ws, FwdBufs* b) {
     b->chunk = c.take<int32_t>(permute_scratch_ints(P, sh->E));
     b->tiles = c.take<FatTile>((size_t)max_fat_tiles(P, sh->E));
     b->units = c.take<ThinUnit>((size_t)max_thin_units(sh->E, thin_unit_tokens(sh->H, sh->I)));
+    b->mma_tiles = c.take<FatTile>((size_t)sh->E);
     b->xy = c.take<__nv_bfloat16>((size_t)(rows_alloc(P) * sh->H));
     b->h = c.take<__nv_bfloat16>((size_t)(rows_alloc(P) * sh->I));
     return align_up(c.off, 256);
@@ -211,28 +251,31 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
                        __nv_bfloat16* h, __nv_bfloat16* y, const Plan& plan,
                        int64_t fat_bound, cudaStream_t s, cudaEvent_t* ev) {
     const int64_t P = (int64_t)sh->T * sh->k;
-    const int thr = sh->fat_threshold;
-    const bool any_fat = fat_bound >= std::max(thr, 1);
-    const bool any_thin = thr > 0;
+    const ExpertKernels kn = expert_kernels(sh, fat_bound);
     const int64_t ra = rows_alloc(P);
-    if (any_fat)
-        CUDA_TRY(launch_gather(x, perm, sh->k, sh->H, plan, x_sorted, dev.num_sms, s), "gather");
+    const int E = sh->E, H = sh->H, I = sh->I, sms = dev.num_sms;
+    if (kn.gather())
+        CUDA_TRY(launch_gather(x, perm, sh->k, H, plan, x_sorted, sms, s), "gather");
     CUDA_TRY(mark(ev, kEvGather, s), "cudaEventRecord");
-    if (any_fat)
-        CUDA_TRY(launch_gemm_gate_up(x_sorted, ra, Wg, Wu, sh->E, sh->H, sh->I, plan, h,
-                                     dev.num_sms, s), "grouped GEMM gate/up");
+    if (kn.fat)
+        CUDA_TRY(launch_gemm_gate_up(x_sorted, ra, Wg, Wu, E, H, I, plan, h, sms, s),
+                 "grouped GEMM gate/up");
     CUDA_TRY(mark(ev, kEvGemmGateUp, s), "cudaEventRecord");
-    if (any_thin)
-        CUDA_TRY(launch_thin_gate_up(x, perm, sh->k, sh->H, sh->I, Wg, Wu, plan, fat_bound, h,
-                                     dev.num_sms, s), "thin gate/up");
+    if (kn.units)
+        CUDA_TRY(launch_thin_gate_up(x, perm, sh->k, H, I, Wg, Wu, plan, fat_bound, h, sms, s),
+                 "thin gate/up");
+    if (kn.mma)
+        CUDA_TRY(launch_thin_mma_gate_up(x_sorted, ra, Wg, Wu, E, H, I, plan, h, sms, s),
+                 "thin gate/up (tensor cores)");
     CUDA_TRY(mark(ev, kEvThinGateUp, s), "cudaEventRecord");
-    if (any_fat)
-        CUDA_TRY(launch_gemm_down(h, ra, Wd, sh->E, sh->H, sh->I, plan, y, dev.num_sms, s),
-                 "grouped GEMM down");
+    if (kn.fat)
+        CUDA_TRY(launch_gemm_down(h, ra, Wd, E, H, I, plan, y, sms, s), "grouped GEMM down");
     CUDA_TRY(mark(ev, kEvGemmDown, s), "cudaEventRecord");
-    if (any_thin)
-        CUDA_TRY(launch_thin_down(h, sh->H, sh->I, Wd, plan, fat_bound, y, dev.num_sms, s),
-                 "thin down");
+    if (kn.units)
+        CUDA_TRY(launch_thin_down(h, H, I, Wd, plan, fat_bound, y, sms, s), "thin down");
+    if (kn.mma)
+        CUDA_TRY(launch_thin_mma_down(h, ra, Wd, E, H, I, plan, y, sms, s),
+                 "thin down (tensor cores)");
     CUDA_TRY(mark(ev, kEvThinDown, s), "cudaEventRecord");
     return MOE_OK;
 }
@@ -304,8 +347,7 @@ moe_status moe_expert_ffn(const moe_shape* shape, const moe_bf16* x, const int32
     DeviceInfo dev;
     if ((st = device_info(&dev)) != MOE_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    Plan plan{b.tiles, b.units, b.hdr, shape->fat_threshold,
-              thin_unit_tokens(shape->H, shape->I)};
+    const Plan plan = make_plan(shape, b.tiles, b.units, b.mma_tiles, b.hdr);
     CUDA_TRY(launch_plan(counts, offsets, shape->E, plan, s), "plan");
     st = run_experts(shape, dev, (const __nv_bfloat16*)x, perm, offsets, counts,
                      (const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
@@ -359,8 +401,7 @@ static moe_status forward_impl(const moe_shape* shape, const float* logits, cons
     CUDA_TRY(mark(ev, kEvStart, s), "cudaEventRecord");
     CUDA_TRY(launch_route(logits, T, E, k, idx, g, s), "route");
     CUDA_TRY(mark(ev, kEvRoute, s), "cudaEventRecord");
-    Plan plan{b.tiles, b.units, b.hdr, shape->fat_threshold,
-              thin_unit_tokens(shape->H, shape->I)};
+    const Plan plan = make_plan(shape, b.tiles, b.units, b.mma_tiles, b.hdr);
     const int64_t P = (int64_t)T * k;
     const int64_t nch = (P + kPermChunk - 1) / kPermChunk;
     CUDA_TRY(launch_permute(idx, T, E, k, b.counts, b.offsets, b.perm, b.inv_perm, b.chunk,
@@ -409,8 +450,11 @@ int32_t moe_forward_launches(const moe_shape* shape) {
     const int64_t P = (int64_t)shape->T * shape->k;
     int32_t n = 1;                                   // route
     n += (P <= kPermChunk) ? 1 : 3;                  // route lists (+ planner)
-    if (shape->T >= std::max(shape->fat_threshold, 1)) n += 3;  // gather, 2 GEMMs
-    if (shape->fat_threshold > 0) n += 2;            // thin gate/up, thin down
+    const ExpertKernels kn = expert_kernels(shape, shape->T);
+    if (kn.gather()) n += 1;
+    if (kn.fat) n += 2;                              // grouped GEMMs
+    if (kn.units) n += 2;                            // CUDA-core streaming
+    if (kn.mma) n += 2;                              // tensor-core streaming
     n += 1;                                          // combine
     return n;
 }

@@ -34,11 +34,13 @@
 
 #include "moe_internal.cuh"
 #include "ptx.cuh"
+#include "tcgen05.cuh"
 
 namespace moe {
 namespace {
 
 using namespace ptx;
+using namespace tc;
 
 constexpr int BM = kTileM;          // 128 rows per tile
 constexpr int BK = 64;              // 64 bf16 = 128 bytes = one swizzle row
@@ -50,69 +52,7 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
 constexpr int TMEM_COLS = 512;                  // two 256-column accumulators
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
-// N >> 3 at bit 17, M >> 4 at bit 24.
-constexpr uint32_t make_idesc(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-constexpr uint32_t kIdesc = make_idesc(BM, BN_MMA);
-
-// Shared-memory matrix descriptor for a K-major tile written by TMA with
-// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);       // start address
-    d |= (uint64_t)1 << 16;                         // leading byte offset (unused)
-    d |= (uint64_t)(1024 >> 4) << 32;               // stride byte offset
-    d |= (uint64_t)1 << 46;                         // descriptor version
-    d |= (uint64_t)2 << 61;                         // 128-byte swizzle
-    return d;
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate));
-}
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
-// 32 lanes x 32 consecutive fp32 columns.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-          "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
-          "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
-          "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-          "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<const uint32_t*>(&v);
-}
+constexpr uint32_t kIdesc = tc::make_idesc(BM, BN_MMA);
 
 struct GemmArgs {
     const FatTile* tiles;
@@ -166,14 +106,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         if (kGated) prefetch_map(&tmB1);
     }
     if (warp == 2) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(tmem_holder)),
-                     "r"(TMEM_COLS));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
     }
-    tc_fence_before();
+    fence_before();
     __syncthreads();
-    tc_fence_after();
+    fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
     const int n_tiles_m = args.hdr_ro->n_fat_tiles;
@@ -235,14 +172,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 ok = false;
                 break;
             }
-            tc_fence_after();
+            fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN_MMA);
             for (int kb = 0; kb < args.k_blocks; ++kb) {
                 if (*abort_flag || !mbar_wait(full_bar(stage), phase)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
+                fence_after();
                 const uint32_t sa = base + stage * STAGE_BYTES;
                 const uint32_t sb = sa + A_BYTES;
                 const uint64_t ad = sw128_desc(sa);
@@ -250,25 +187,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     // +32 bytes per 16-element K step inside the swizzle row
-                    umma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
-                              (kb > 0 || kk > 0) ? 1u : 0u);
+                    mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), kIdesc,
+                             (kb > 0 || kk > 0) ? 1u : 0u);
                 }
                 issued = true;
-                umma_commit(empty_bar(stage));
+                commit(empty_bar(stage));
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) break;
-            umma_commit(tfull_bar(acc));
+            commit(tfull_bar(acc));
         }
         if (!ok) {
             *abort_flag = 1;
             set_status(args.hdr, MOE_ERR_TIMEOUT);
             if (issued) {
                 // Wait for every MMA issued so far before TMEM is freed.
-                umma_commit(done_bar);
+                commit(done_bar);
                 (void)mbar_wait(done_bar, 0);
             }
         }
@@ -285,7 +222,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 set_status(args.hdr, MOE_ERR_TIMEOUT);
                 break;
             }
-            tc_fence_after();
+            fence_after();
             const int mt = t / args.n_blocks_n;
             const int nt = t % args.n_blocks_n;
             const FatTile ft = args.tiles[mt];
@@ -305,9 +242,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     for (int q = 0; q < 16; ++q) {
                         const float g0 = __uint_as_float(g[2 * q]), g1 = __uint_as_float(g[2 * q + 1]);
                         const float u0 = __uint_as_float(u[2 * q]), u1 = __uint_as_float(u[2 * q + 1]);
-                        const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
-                        const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
-                        packed[q] = pack_bf16(h0, h1);
+                        packed[q] = pack_bf16(swiglu(g0, u0), swiglu(g1, u1));
                     }
                     if (valid) {
                         uint4* d4 = reinterpret_cast<uint4*>(dst + c);
@@ -336,17 +271,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     }
                 }
             }
-            tc_fence_before();
+            fence_before();
             mbar_arrive(tempty_bar(acc));
         }
     }
 
-    tc_fence_before();
+    fence_before();
     __syncthreads();
     if (warp == 2) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                     "r"(TMEM_COLS));
+        fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
@@ -371,22 +305,6 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D bf16 map over a row-major [rows, cols] matrix, box = 64 cols x box_rows,
-// 128-byte swizzle, zero fill outside the tensor.
-cudaError_t make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
-                     uint32_t box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return cudaErrorNotSupported;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <bool kGated>
 cudaError_t set_smem_attr() {
     static cudaError_t err = cudaErrorUnknown;
@@ -400,15 +318,29 @@ cudaError_t set_smem_attr() {
 
 }  // namespace
 
+cudaError_t make_tma_map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                              uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64u, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_gemm_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_alloc,
                                 const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
                                 int E, int H, int I, const Plan& plan,
                                 __nv_bfloat16* h, int num_sms, cudaStream_t s) {
     CUtensorMap mA, mG, mU;
     cudaError_t e;
-    if ((e = make_map(&mA, x_sorted, (uint64_t)rows_alloc, (uint64_t)H, BM)) != cudaSuccess) return e;
-    if ((e = make_map(&mG, Wg, (uint64_t)E * I, (uint64_t)H, 128)) != cudaSuccess) return e;
-    if ((e = make_map(&mU, Wu, (uint64_t)E * I, (uint64_t)H, 128)) != cudaSuccess) return e;
+    if ((e = make_tma_map_bf16(&mA, x_sorted, (uint64_t)rows_alloc, (uint64_t)H, BM)) != cudaSuccess) return e;
+    if ((e = make_tma_map_bf16(&mG, Wg, (uint64_t)E * I, (uint64_t)H, 128)) != cudaSuccess) return e;
+    if ((e = make_tma_map_bf16(&mU, Wu, (uint64_t)E * I, (uint64_t)H, 128)) != cudaSuccess) return e;
     if ((e = set_smem_attr<true>()) != cudaSuccess) return e;
     GemmArgs a;
     a.tiles = plan.tiles;
@@ -430,8 +362,8 @@ cudaError_t launch_gemm_down(const __nv_bfloat16* h, int64_t rows_alloc,
                              int num_sms, cudaStream_t s) {
     CUtensorMap mA, mD;
     cudaError_t e;
-    if ((e = make_map(&mA, h, (uint64_t)rows_alloc, (uint64_t)I, BM)) != cudaSuccess) return e;
-    if ((e = make_map(&mD, Wd, (uint64_t)E * H, (uint64_t)I, 256)) != cudaSuccess) return e;
+    if ((e = make_tma_map_bf16(&mA, h, (uint64_t)rows_alloc, (uint64_t)I, BM)) != cudaSuccess) return e;
+    if ((e = make_tma_map_bf16(&mD, Wd, (uint64_t)E * H, (uint64_t)I, 256)) != cudaSuccess) return e;
     if ((e = set_smem_attr<false>()) != cudaSuccess) return e;
     GemmArgs a;
     a.tiles = plan.tiles;

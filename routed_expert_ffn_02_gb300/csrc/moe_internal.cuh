@@ -25,7 +25,8 @@ struct WsHeader {
     int32_t n_fat_tiles;   // grouped-GEMM row tiles built by the planner
     int32_t n_thin;        // work units on the weight-streaming path
     int32_t thin_weight;   // sum of thin_unit_cost over those units
-    int32_t reserved[60];
+    int32_t n_thin_mma;    // thin experts on the tensor-core streaming kernel
+    int32_t reserved[59];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -55,14 +56,25 @@ __host__ __device__ inline int thin_unit_cost(int n) { return (n < 4 ? 4 : n) + 
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Planner outputs (the split of experts between the two expert paths).
+// Planner outputs (the split of experts between the expert kernels).  A thin
+// expert (0 < count < fat_threshold) with at least thin_mma_min slots streams
+// its weights through the tensor cores (one FatTile of <= kThinMaxTokens rows
+// in mma_tiles); the others take the CUDA-core streaming kernel (units).
 struct Plan {
     FatTile* tiles;      // [max_fat_tiles(P, E)]
     ThinUnit* units;     // [max_thin_units(E, unit_tokens)], expert-major
+    FatTile* mma_tiles;  // [E]
     WsHeader* hdr;
     int32_t fat_threshold;
     int32_t unit_tokens; // slots per weight-streaming unit (thin_unit_tokens)
+    int32_t thin_mma_min;
 };
+
+// By default every thin expert streams on the tensor cores once at least this
+// many 128-row gate/up work items can exist (touched experts x I/128), and
+// on CUDA cores below it.  Measured on GB300 (H=4096, I=2048): decode batch 2
+// (<= 256 items) is faster on CUDA cores, batch 4 (<= 512) on tensor cores.
+constexpr int kThinMmaAutoItems = 384;
 
 inline int64_t max_fat_tiles(int64_t P, int E) { return P / kTileM + E + 1; }
 inline int64_t max_thin_units(int E, int unit_tokens) {
@@ -101,6 +113,17 @@ cudaError_t launch_thin_gate_up(const __nv_bfloat16* x, const int32_t* perm, int
 cudaError_t launch_thin_down(const __nv_bfloat16* h, int H, int I, const __nv_bfloat16* Wd,
                              const Plan& plan, int64_t max_slots, __nv_bfloat16* y_sorted,
                              int num_sms, cudaStream_t s);
+
+// Weight streaming on tcgen05 for the thin experts in plan.mma_tiles:
+// gate_up: h[rows] = silu(x_sorted[rows] Wg_e^T) * (x_sorted[rows] Wu_e^T);
+// down: y[rows] = h[rows] Wd_e^T.  x_sorted / h hold rows_alloc rows.
+cudaError_t launch_thin_mma_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_alloc,
+                                    const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int E,
+                                    int H, int I, const Plan& plan, __nv_bfloat16* h,
+                                    int num_sms, cudaStream_t s);
+cudaError_t launch_thin_mma_down(const __nv_bfloat16* h, int64_t rows_alloc,
+                                 const __nv_bfloat16* Wd, int E, int H, int I, const Plan& plan,
+                                 __nv_bfloat16* y_sorted, int num_sms, cudaStream_t s);
 
 // Grouped GEMMs on tcgen05.  gate_up: h = silu(A Wg^T) * (A Wu^T) for the
 // fat tiles, A = x_sorted [rows_alloc, H].  down: y = h Wd^T, A = h.

@@ -68,27 +68,32 @@ __device__ int block_exclusive_scan(int* a, int n, int* ws) {
 }
 
 // Planner: fat experts (count >= threshold, count > 0) get ceil(count/128)
-// row tiles; thin experts (0 < count < threshold) get ceil(count/unit_tokens)
-// weight-streaming units, each with the running sum of unit costs before it
-// (thin_unit_cost) so the streaming kernels can split rows evenly by cost.
+// row tiles; thin experts (0 < count < threshold) with at least thin_mma_min
+// slots get one tile for the tensor-core streaming kernel; the other thin
+// experts get ceil(count/unit_tokens) CUDA-core streaming units, each with the
+// running sum of unit costs before it (thin_unit_cost) so that kernel can
+// split rows evenly by cost.
 // cnt/off: shared copies of counts/offsets; ta, tb: shared int[E] scratch.
 template <int NT>
 __device__ void block_plan(const int* cnt, const int* off, int E, const Plan& plan,
                            int* ta, int* tb, int* ws) {
     const int thr = plan.fat_threshold;
     const int nu = plan.unit_tokens;
+    const int mma_min = plan.thin_mma_min;
+    auto is_fat = [&](int c) { return c > 0 && c >= thr; };
+    auto is_mma = [&](int c) { return c > 0 && c < thr && c >= mma_min; };
+    auto is_unit = [&](int c) { return c > 0 && c < thr && c < mma_min; };
     for (int e = threadIdx.x; e < E; e += NT) {
         const int c = cnt[e];
-        const bool fat = c > 0 && c >= thr;
-        ta[e] = fat ? (c + kTileM - 1) / kTileM : 0;
-        tb[e] = (c > 0 && c < thr) ? (c + nu - 1) / nu : 0;
+        ta[e] = is_fat(c) ? (c + kTileM - 1) / kTileM : 0;
+        tb[e] = is_mma(c) ? 1 : 0;
     }
     __syncthreads();
     const int n_tiles = block_exclusive_scan<NT>(ta, E, ws);
-    const int n_units = block_exclusive_scan<NT>(tb, E, ws);
+    const int n_mma = block_exclusive_scan<NT>(tb, E, ws);
     for (int e = threadIdx.x; e < E; e += NT) {
         const int c = cnt[e];
-        if (c > 0 && c >= thr) {
+        if (is_fat(c)) {
             const int nt = (c + kTileM - 1) / kTileM;
             for (int i = 0; i < nt; ++i) {
                 FatTile ft;
@@ -98,22 +103,31 @@ __device__ void block_plan(const int* cnt, const int* off, int E, const Plan& pl
                 ft.pad = 0;
                 plan.tiles[ta[e] + i] = ft;
             }
+        } else if (is_mma(c)) {
+            FatTile ft;
+            ft.expert = e;
+            ft.row0 = off[e];
+            ft.rows = c;
+            ft.pad = 0;
+            plan.mma_tiles[tb[e]] = ft;
         }
     }
-    // Unit costs: reuse ta as each thin expert's total cost, scanned.
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += NT) {
         const int c = cnt[e];
+        tb[e] = is_unit(c) ? (c + nu - 1) / nu : 0;
+        // unit costs of the expert, scanned below
         int w = 0;
-        if (c > 0 && c < thr)
+        if (is_unit(c))
             for (int i = 0; i * nu < c; ++i) w += thin_unit_cost(min(nu, c - i * nu));
         ta[e] = w;
     }
     __syncthreads();
+    const int n_units = block_exclusive_scan<NT>(tb, E, ws);
     const int weight = block_exclusive_scan<NT>(ta, E, ws);
     for (int e = threadIdx.x; e < E; e += NT) {
         const int c = cnt[e];
-        if (c > 0 && c < thr) {
+        if (is_unit(c)) {
             int before = ta[e];
             for (int i = 0; i * nu < c; ++i) {
                 ThinUnit u;
@@ -130,6 +144,7 @@ __device__ void block_plan(const int* cnt, const int* off, int E, const Plan& pl
         plan.hdr->n_fat_tiles = n_tiles;
         plan.hdr->n_thin = n_units;
         plan.hdr->thin_weight = weight;
+        plan.hdr->n_thin_mma = n_mma;
     }
 }
 
@@ -328,20 +343,23 @@ plan_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ offs
     block_plan<1024>(cnt, off, E, plan, ta, tb, ws);
 }
 
-// x_sorted[p] = x[perm[p] / k] for the rows of the fat tiles; one warp per
-// row, 16-byte vectors.
+// x_sorted[p] = x[perm[p] / k] for the rows of the fat tiles and of the
+// tensor-core streaming tiles; one warp per row, 16-byte vectors.
 __global__ void __launch_bounds__(256)
 gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
               int k, int H, const FatTile* __restrict__ tiles,
+              const FatTile* __restrict__ mma_tiles,
               const WsHeader* __restrict__ hdr, uint4* __restrict__ x_sorted) {
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    const int64_t rows = (int64_t)hdr->n_fat_tiles * kTileM;
+    const int64_t fat_rows = (int64_t)hdr->n_fat_tiles * kTileM;
+    const int64_t rows = fat_rows + (int64_t)hdr->n_thin_mma * kThinMaxTokens;
     const int vec = H / 8;
     for (int64_t r = warp; r < rows; r += nwarps) {
-        const FatTile ft = tiles[r / kTileM];
-        const int i = (int)(r % kTileM);
+        const FatTile ft = r < fat_rows ? tiles[r / kTileM]
+                                        : mma_tiles[(r - fat_rows) / kThinMaxTokens];
+        const int i = r < fat_rows ? (int)(r % kTileM) : (int)((r - fat_rows) % kThinMaxTokens);
         if (i >= ft.rows) continue;
         const int64_t p = ft.row0 + i;
         const int64_t t = perm[p] / k;
@@ -390,7 +408,7 @@ cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* perm, int k,
                           int H, const Plan& plan, __nv_bfloat16* x_sorted,
                           int num_sms, cudaStream_t s) {
     gather_kernel<<<num_sms * 8, 256, 0, s>>>(
-        reinterpret_cast<const uint4*>(x), perm, k, H, plan.tiles, plan.hdr,
+        reinterpret_cast<const uint4*>(x), perm, k, H, plan.tiles, plan.mma_tiles, plan.hdr,
         reinterpret_cast<uint4*>(x_sorted));
     return cudaGetLastError();
 }

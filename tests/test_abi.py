@@ -55,6 +55,7 @@ def test_workspace_sizes(moe):
 @pytest.mark.parametrize("bad", [
     dict(T=-1), dict(E=0), dict(E=1025), dict(k=0), dict(k=9), dict(E=4, k=5),
     dict(H=100), dict(H=0), dict(I=128), dict(fat_threshold=-1), dict(fat_threshold=34),
+    dict(thin_mma_min=-1), dict(thin_mma_min=34),
 ])
 def test_bad_shapes_rejected(moe, bad):
     base = dict(T=16, E=16, k=2, H=512, I=256, fat_threshold=32)
@@ -131,3 +132,19 @@ def test_stager_argument_errors(moe):
     assert lib.moe_stager_create(ctypes.c_void_p(0x10010), 2, 1 << 20, ctypes.byref(h)) == 1
     assert lib.moe_forward_offload(None, ctypes.byref(shape), 1, None, None, None, None, None, 0,
                                    None, None) == 1
+
+
+def test_forward_launch_count(moe):
+    """Kernels one moe_forward launches: route, route lists (1 or 3), then
+    only the expert kernels that can have work, then combine."""
+    S = moe.Shape
+    # decode: 8 or 16 touched experts x 16 blocks < 384 items -> CUDA cores
+    assert moe.forward_launches(S(1, 384, 8, 4096, 2048)) == 5
+    assert moe.forward_launches(S(2, 384, 8, 4096, 2048)) == 5
+    assert moe.forward_launches(S(3, 384, 8, 4096, 2048)) == 6       # 24 x 16 = 384: tensor cores
+    assert moe.forward_launches(S(1, 384, 8, 4096, 2048, thin_mma_min=1)) == 6
+    assert moe.forward_launches(S(4, 384, 8, 4096, 2048, thin_mma_min=33)) == 5
+    assert moe.forward_launches(S(16384, 384, 8, 4096, 2048)) == 10
+    assert moe.forward_launches(S(16384, 384, 8, 4096, 2048, thin_mma_min=8)) == 12
+    assert moe.forward_launches(S(16384, 384, 8, 4096, 2048, fat_threshold=0)) == 8
+    assert moe.forward_launches(S(0, 384, 8, 4096, 2048)) == 0

@@ -44,26 +44,34 @@ def _forward(moe, shape, d, profiled=False):
     return out, idx, gates
 
 
-def _full_check(moe, s, thr, inp, d=None):
+# thin_mma_min values: 1 = every thin expert on the tensor-core streaming
+# kernel, 33 = every thin expert on the CUDA-core one (0 = chosen by shape).
+MMA_ALL, MMA_NONE = 1, 33
+
+
+def _full_check(moe, s, thr, inp, d=None, mma_min=0):
     d = d or _to_dev(inp)
-    shape = moe.Shape(s.T, s.E, s.k, s.H, s.I, fat_threshold=thr)
+    shape = moe.Shape(s.T, s.E, s.k, s.H, s.I, fat_threshold=thr, thin_mma_min=mma_min)
     out, idx, gates = _forward(moe, shape, d)
     experts = DeviceExperts(d["Wg"], d["Wu"], d["Wd"])
     ref, ridx, rgates = oracle_rows(synth.bf16_bits(inp["x"]), inp["logits"].numpy(), s.k,
                                     experts, np.arange(s.T))
     assert np.array_equal(idx.cpu().numpy(), ridx)
     assert np.allclose(gates.cpu().numpy(), rgates, rtol=0, atol=GATE_ATOL)
-    return assert_close(out, ref, f"forward {s} thr={thr}")
+    return assert_close(out, ref, f"forward {s} thr={thr} mma_min={mma_min}")
 
 
 # ---------------------------------------------------------------- tiny layer
 
+@pytest.mark.parametrize("mma_min", [MMA_ALL, 7, MMA_NONE])
 @pytest.mark.parametrize("thr", [0, 1, 8, 32, 33])
-def test_forward_tiny(moe, thr):
+def test_forward_tiny(moe, thr, mma_min):
     """T=64, E=16, top-2, H=512, I=256 (seed 0).  thr=0 sends every expert to
-    the tcgen05 GEMM, thr=32/33 every expert to the weight-streaming path."""
+    the tcgen05 GEMM, thr=32/33 every expert to the weight-streaming path;
+    mma_min splits the thin experts (5..13 slots here) between the two
+    streaming kernels."""
     inp = synth.make_layer(synth.TINY, seed=0)
-    _full_check(moe, synth.TINY, thr, inp)
+    _full_check(moe, synth.TINY, thr, inp, mma_min=mma_min)
 
 
 def test_expert_ffn_and_combine_entry_points(moe):
@@ -117,20 +125,22 @@ def _assigned_logits(counts, E):
     return torch.from_numpy(lg)
 
 
-def test_forward_threshold_edges(moe):
+@pytest.mark.parametrize("mma_min", [MMA_ALL, 31, MMA_NONE])
+def test_forward_threshold_edges(moe, mma_min):
     """Experts with exactly 0, 1, 31, 32, 33, 128, 129 and 255 slots: the
-    fat-threshold boundary and ragged GEMM tiles."""
+    fat-threshold boundary and ragged GEMM tiles (mma_min=31: only the
+    31-slot expert streams on the tensor cores)."""
     counts = [31, 32, 33, 0, 1, 128, 129, 255]
     E = len(counts)
     lg = _assigned_logits(counts, E)
     s = synth.Shape(T=lg.shape[0], E=E, k=1, H=256, I=256)
     inp = synth.make_layer(s, seed=6)
     inp["logits"] = lg
-    rr, _ = _full_check(moe, s, 32, inp)
+    _full_check(moe, s, 32, inp, mma_min=mma_min)
     # k = 2 on the same tokens
     s2 = synth.Shape(T=lg.shape[0], E=E, k=2, H=256, I=256)
     inp["logits"] = lg
-    _full_check(moe, s2, 32, inp)
+    _full_check(moe, s2, 32, inp, mma_min=mma_min)
 
 
 def test_forward_one_expert_takes_all(moe):
@@ -173,13 +183,14 @@ def big_layer():
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("mma_min", [MMA_ALL, MMA_NONE])
 @pytest.mark.parametrize("B", [1, 4])
-def test_forward_decode(moe, big_layer, B):
+def test_forward_decode(moe, big_layer, B, mma_min):
     s = synth.Shape(T=B, E=384, k=8, H=4096, I=2048)
     inp = dict(x=synth.make_x(B, s.H, seed=0), logits=synth.make_logits(B, s.E, seed=0,
                                                                            zipf_s=synth.ZIPF_S))
     d = dict(_to_dev(inp), **big_layer)
-    _full_check(moe, s, 32, inp, d)
+    _full_check(moe, s, 32, inp, d, mma_min=mma_min)
 
 
 def _sample_tokens(idx_np, counts_np, thr, rng, n_random=24):
@@ -201,8 +212,9 @@ def _sample_tokens(idx_np, counts_np, thr, rng, n_random=24):
     return np.array(sorted(picks))
 
 
-@pytest.mark.parametrize("H,I", [(4096, 2048), (2048, 1024)])
-def test_forward_prefill_sampled(moe, big_layer, H, I):
+@pytest.mark.parametrize("H,I,mma_min", [(4096, 2048, 0), (4096, 2048, MMA_NONE),
+                                         (2048, 1024, 0)])
+def test_forward_prefill_sampled(moe, big_layer, H, I, mma_min):
     """16,384-token chunk, Zipf(1.1)-skewed routing.  Routing, counts and the
     permutation are checked on all tokens; outputs on a sample covering random
     tokens, tokens of thin experts and of the smallest and hottest fat expert."""
@@ -215,7 +227,7 @@ def test_forward_prefill_sampled(moe, big_layer, H, I):
         Wg, Wu, Wd = synth.make_weights(s.E, H, I, seed=0, layer=0, device="cuda")
         W = dict(Wg=Wg, Wu=Wu, Wd=Wd)
     d = dict(_to_dev(inp), **W)
-    shape = moe.Shape(s.T, s.E, s.k, H, I, fat_threshold=32)
+    shape = moe.Shape(s.T, s.E, s.k, H, I, fat_threshold=32, thin_mma_min=mma_min)
     out, idx, gates = _forward(moe, shape, d)
     lg = inp["logits"].numpy()
     ridx, rgates = oracle.route(lg, s.k)
@@ -230,7 +242,7 @@ def test_forward_prefill_sampled(moe, big_layer, H, I):
     toks = _sample_tokens(ridx, rc, 32, np.random.default_rng(1))
     experts = DeviceExperts(W["Wg"], W["Wu"], W["Wd"])
     ref, _, _ = oracle_rows(synth.bf16_bits(inp["x"]), lg, s.k, experts, toks)
-    assert_close(out[torch.from_numpy(toks).cuda()], ref, f"prefill H={H}")
+    assert_close(out[torch.from_numpy(toks).cuda()], ref, f"prefill H={H} mma_min={mma_min}")
 
 
 def test_forward_deterministic_and_profiled(moe, big_layer):
@@ -268,21 +280,23 @@ def test_decode_sweep_four_layers(moe):
 
 @pytest.mark.parametrize("T,E,k,H,I", [(40, 8, 2, 768, 512), (20, 4, 4, 256, 768),
                                        (70, 6, 3, 1280, 256), (33, 33, 1, 2048, 1024)])
-@pytest.mark.parametrize("thr", [0, 33])
-def test_forward_odd_shapes(moe, T, E, k, H, I, thr):
-    """Hidden sizes that are not powers of two, both expert paths."""
+@pytest.mark.parametrize("thr,mma_min", [(0, 0), (33, MMA_ALL), (33, MMA_NONE)])
+def test_forward_odd_shapes(moe, T, E, k, H, I, thr, mma_min):
+    """Hidden sizes that are not powers of two, all three expert kernels."""
     s = synth.Shape(T=T, E=E, k=k, H=H, I=I)
-    _full_check(moe, s, thr, synth.make_layer(s, seed=T, zipf_s=synth.ZIPF_S))
+    _full_check(moe, s, thr, synth.make_layer(s, seed=T, zipf_s=synth.ZIPF_S), mma_min=mma_min)
 
 
-def test_thin_units_split_at_full_width(moe):
+@pytest.mark.parametrize("mma_min", [MMA_NONE, 13, MMA_ALL])
+def test_thin_units_split_at_full_width(moe, mma_min):
     """Full-width experts (H=4096, I=2048) with 1..32 slots on the weight-
-    streaming path (threshold 33): experts with more slots than one unit
-    holds are split into several units, each streaming the weights again."""
+    streaming path (threshold 33).  On CUDA cores, experts with more slots
+    than one unit holds are split into several units, each streaming the
+    weights again; on the tensor cores one tile holds up to 32 slots."""
     counts = [1, 12, 13, 24, 25, 31, 32, 2]
     E = len(counts)
     lg = _assigned_logits(counts, E)
     s = synth.Shape(T=lg.shape[0], E=E, k=1, H=4096, I=2048)
     inp = synth.make_layer(s, seed=8)
     inp["logits"] = lg
-    _full_check(moe, s, 33, inp)
+    _full_check(moe, s, 33, inp, mma_min=mma_min)
