@@ -256,6 +256,44 @@ moe_status moe_forward_offload(moe_stager* stager, const moe_shape* shape, int32
                                void* ws, size_t ws_bytes, moe_stream_t compute,
                                moe_stream_t copy);
 
+/* ---- activations in host memory --------------------------------------- */
+
+/* The layer on host-resident activations, as a serving process feeds it:
+ * every call copies its logits and x in from host memory, runs moe_forward
+ * and copies out back, and successive calls on one pipe overlap (call i's
+ * inputs arrive and call i-2's output leaves while call i-1 computes).  Not
+ * on the pages: their layer's activations already live on the GPU. */
+typedef struct moe_pipe moe_pipe;
+
+/* Bytes of device workspace moe_forward_host needs: moe_workspace_size()
+ * plus two staging slots of x [T, H] bf16, logits [T, E] fp32 and
+ * out [T, H] bf16 (0 for an invalid shape). */
+size_t moe_pipe_workspace_size(const moe_shape* shape);
+
+/* A pipe owns six CUDA events and a call counter, no device memory. */
+moe_status moe_pipe_create(moe_pipe** out);
+moe_status moe_pipe_destroy(moe_pipe* pipe);
+
+/* moe_forward with logits_h [T, E] fp32, x_h [T, H] bf16 and out_h [T, H]
+ * bf16 in host memory (pinned, or the copies serialise with the host).
+ * Call i stages through slot i mod 2 at the end of ws:
+ *   h2d:     once call i-2's compute has read the slot's inputs, copy
+ *            logits_h and x_h in;
+ *   compute: once they have landed and call i-2's output has left the slot,
+ *            moe_forward into the slot;
+ *   d2h:     once that is done, copy the slot's out to out_h.
+ * Asynchronous: out_h is complete when `d2h` passes that copy (synchronise
+ * d2h).  The three streams must differ; every call on a pipe uses the same
+ * shape, ws (moe_pipe_workspace_size bytes, moe_workspace_init'ed) and
+ * streams; host buffers must stay valid until their copies are done.
+ * Errors: as moe_forward, plus MOE_ERR_INVALID_ARG for a NULL pipe or host
+ * buffer or equal streams. */
+moe_status moe_forward_host(moe_pipe* pipe, const moe_shape* shape, const float* logits_h,
+                            const moe_bf16* x_h, const moe_bf16* W_gate, const moe_bf16* W_up,
+                            const moe_bf16* W_down, moe_bf16* out_h, void* ws,
+                            size_t ws_bytes, moe_stream_t compute, moe_stream_t h2d,
+                            moe_stream_t d2h);
+
 /* ---- workspace status ---------------------------------------------- */
 
 /* Clears the status word of a fresh workspace (asynchronous on stream). */

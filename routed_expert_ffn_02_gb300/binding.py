@@ -36,7 +36,9 @@ EXPORTED = ("moe_route", "moe_permute_workspace_size", "moe_permute", "moe_permu
             "moe_workspace_size", "moe_forward", "moe_forward_profiled",
             "moe_forward_launches", "moe_layer_weight_bytes", "moe_stager_create",
             "moe_stager_destroy", "moe_forward_offload", "moe_workspace_init",
-            "moe_workspace_status", "moe_last_error", "moe_version")
+            "moe_workspace_status", "moe_last_error", "moe_version",
+            "moe_pipe_workspace_size", "moe_pipe_create", "moe_pipe_destroy",
+            "moe_forward_host")
 
 
 class MoeShape(ctypes.Structure):
@@ -96,6 +98,10 @@ _sig = {
     "moe_forward_offload": ([_P, _SP, _i32, ctypes.POINTER(_P), _P, ctypes.POINTER(_P),
                              ctypes.POINTER(_P), _P, _sz, _P, _P], _i32),
     "moe_workspace_init": ([_P, _sz, _P], _i32),
+    "moe_pipe_workspace_size": ([_SP], _sz),
+    "moe_pipe_create": ([ctypes.POINTER(_P)], _i32),
+    "moe_pipe_destroy": ([_P], _i32),
+    "moe_forward_host": ([_P, _SP, _P, _P, _P, _P, _P, _P, _P, _sz, _P, _P, _P], _i32),
     "moe_workspace_status": ([_P, _P, _i32], _i32),
     "moe_last_error": ([], ctypes.c_char_p),
     "moe_version": ([], ctypes.c_char_p),
@@ -110,6 +116,11 @@ def _ptr(t: torch.Tensor | None):
     if t is None:
         return None
     assert t.is_cuda and t.is_contiguous(), "expected a contiguous CUDA tensor"
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host_ptr(t: torch.Tensor):
+    assert not t.is_cuda and t.is_contiguous(), "expected a contiguous host tensor"
     return ctypes.c_void_p(t.data_ptr())
 
 
@@ -332,6 +343,56 @@ class Stager:
                                         ws.ptr, ws.nbytes, ctypes.c_void_p(compute.cuda_stream),
                                         ctypes.c_void_p(copy.cuda_stream)), "moe_forward_offload")
         return outs
+
+
+def pipe_workspace_size(shape: Shape) -> int:
+    n = _lib.moe_pipe_workspace_size(ctypes.byref(shape.c()))
+    if n == 0:
+        raise MoeError(1, "moe_pipe_workspace_size")
+    return n
+
+
+class Pipe:
+    """The layer on activations in host memory: each forward() copies its
+    inputs in on an h2d stream, computes on `compute` and copies the output
+    back on a d2h stream, overlapping with the neighbouring calls.  Owns the
+    library pipe, its workspace (with two staging slots) and the two copy
+    streams; all calls use one shape and one compute stream."""
+
+    def __init__(self, shape: Shape, device=None, compute=None):
+        device = device or torch.device("cuda", torch.cuda.current_device())
+        self.shape = shape
+        self.compute = compute if compute is not None else torch.cuda.current_stream(device)
+        self.h2d = torch.cuda.Stream(device=device)
+        self.d2h = torch.cuda.Stream(device=device)
+        self.ws = Workspace(pipe_workspace_size(shape), device, self.compute)
+        self._h = ctypes.c_void_p()
+        _check(_lib.moe_pipe_create(ctypes.byref(self._h)), "moe_pipe_create")
+
+    def close(self):
+        if self._h:
+            _lib.moe_pipe_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def forward(self, logits_h, x_h, W_gate, W_up, W_down, out_h):
+        """Enqueues one layer: logits_h [T, E] fp32, x_h [T, H] bf16 and
+        out_h [T, H] bf16 are (pinned) host tensors; out_h is written when
+        the d2h stream reaches it (see synchronize())."""
+        _check(_lib.moe_forward_host(self._h, ctypes.byref(self.shape.c()), _host_ptr(logits_h),
+                                     _host_ptr(x_h), _ptr(W_gate), _ptr(W_up), _ptr(W_down),
+                                     _host_ptr(out_h), self.ws.ptr, self.ws.nbytes,
+                                     _stream(self.compute), _stream(self.h2d),
+                                     _stream(self.d2h)), "moe_forward_host")
+        return out_h
+
+    def synchronize(self):
+        self.d2h.synchronize()
 
 
 def raw_lib():

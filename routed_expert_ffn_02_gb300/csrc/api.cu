@@ -110,6 +110,12 @@ moe_status check_shape(const moe_shape* sh) {
 // enough thin experts to fill the GPU; below that the CUDA-core kernel, which
 // splits weight rows finely over all SMs, is faster.  At most min(E, T*k)
 // experts are touched.
+}  // namespace
+
+moe_status moe::check_shape_status(const moe_shape* shape) { return check_shape(shape); }
+
+namespace {
+
 int thin_mma_min(const moe_shape* sh) {
     if (sh->thin_mma_min > 0) return sh->thin_mma_min;
     const int64_t touched = std::min<int64_t>(sh->E, (int64_t)sh->T * sh->k);

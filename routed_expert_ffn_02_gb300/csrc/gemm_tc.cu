@@ -1,5 +1,5 @@
 // gemm_tc.cu -- grouped expert GEMMs for "busy" experts on the 5th-generation
-// tensor cores (tcgen05 + TMEM), fed by TMA.
+// tensor cores (tcgen05 + TMEM), fed by TMA, on CTA pairs.
 //
 // Experts holding at least the fat threshold of slots run as dense GEMMs
 // (dsv41-flash-offload wiki, overview: busy experts run as FP16 GEMMs; model
@@ -8,20 +8,26 @@
 //
 //   gate/up:  h[rows, n0:n0+128] = silu(A Wg_e[n0:n0+128]^T) * (A Wu_e[n0:n0+128]^T)
 //             A = x_sorted[rows, :H]; one MMA of N = 256 covers the gate and
-//             up halves, which TMA places back to back in shared memory, so
-//             SiLU*up is fused into the epilogue.
+//             up halves, so SiLU*up is fused into the epilogue.
 //   down:     y[rows, n0:n0+256] = h[rows, :I] Wd_e[n0:n0+256]^T
 //
-// The row tiles (128 slots of one expert) come from the planner in device
-// memory, so there is no host synchronisation.  Each CTA is persistent
-// (one per SM) and warp-specialised:
-//   warp 0      TMA producer (one lane): A and B tiles, 64-wide K blocks,
-//               128-byte swizzle, 4-stage ring guarded by mbarriers;
-//   warp 1      MMA issuer (one lane): tcgen05.mma kind::f16, M=128, N=256,
-//               K=16, fp32 accumulators in TMEM, two accumulator buffers
-//               (2 x 256 columns) so the epilogue of one tile overlaps the
-//               main loop of the next;
-//   warp 2      TMEM allocator;
+// Each work item is a 256 x 256 output tile computed by a cluster of two
+// CTAs (tcgen05 cta_group::2, M = 256): CTA r of the pair loads its own
+// 128 rows of A (planner tile 2q + r of the expert) and half of the B tile
+// (gate rows / up rows for gate/up, the first / second 128 weight rows for
+// down), so each SM reads 32 KB from L2 per 64-wide K block instead of the
+// 48 KB a one-CTA 128 x 256 tile needs, and six stages fit in shared memory.
+// Both CTAs' copies complete on the even CTA's "full" barrier; the even CTA
+// issues the MMAs, whose commits arrive on the "empty" and "accumulator
+// full" barriers of both CTAs; each CTA's epilogue reads its own 128 TMEM
+// lanes and releases the accumulator on the even CTA's barrier.
+//
+// Roles per CTA (persistent, one cluster per SM pair):
+//   warp 0      TMA producer (one lane);
+//   warp 1      MMA issuer (one lane, even CTA only): M=256, N=256, K=16,
+//               fp32 accumulators in TMEM, two 256-column buffers so the
+//               epilogue of one tile overlaps the main loop of the next;
+//   warp 2      TMEM allocator (both CTAs, collectively);
 //   warps 4-7   epilogue: tcgen05.ld -> activation -> bf16 -> global.
 // Rows of a tile past the expert's end belong to other experts (or are past
 // the tensor and zero-filled by TMA); they are computed and discarded.
@@ -30,6 +36,7 @@
 // MOE_ERR_TIMEOUT in the workspace status, stops issuing work, waits (bounded)
 // for its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
+#include <algorithm>
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -42,32 +49,36 @@ namespace {
 using namespace ptx;
 using namespace tc;
 
-constexpr int BM = kTileM;          // 128 rows per tile
+constexpr int BM = kTileM;          // A rows per CTA (M = 2 * BM per pair)
 constexpr int BK = 64;              // 64 bf16 = 128 bytes = one swizzle row
-constexpr int BN_MMA = 256;         // MMA N
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;            // 16 KB
-constexpr int B_BYTES = BN_MMA * BK * 2;        // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
-constexpr int TMEM_COLS = 512;                  // two 256-column accumulators
+constexpr int BN_MMA = 256;         // MMA N (each CTA holds BN_MMA / 2 rows of B)
+constexpr int STAGES = 7;
+constexpr int A_BYTES = BM * BK * 2;                // 16 KB
+constexpr int B_BYTES = (BN_MMA / 2) * BK * 2;      // 16 KB (this CTA's half)
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;      // 32 KB
+constexpr int TMEM_COLS = 512;                      // two 256-column accumulators
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
-constexpr uint32_t kIdesc = tc::make_idesc(BM, BN_MMA);
+constexpr uint32_t kIdesc = tc::make_idesc(2 * BM, BN_MMA);
+constexpr uint16_t kPairMask = 0x3;
 
 struct GemmArgs {
-    const FatTile* tiles;
+    const FatTile* tiles;  // pairs: tiles 2q, 2q+1 belong to one expert
     const WsHeader* hdr_ro;
     WsHeader* hdr;
     int n_blocks_n;        // N tiles per expert
     int k_blocks;          // K / 64
-    int b_rows_per_expert; // rows of the B tensor per expert (I or H)
+    int b_rows_per_expert; // rows of the B tensor(s) per expert (I or H)
+    int b_half_rows;       // B row offset of the odd CTA's half (0 gated: own tensor)
     int bn_out;            // output columns per tile (128 gated, 256 down)
     __nv_bfloat16* out;    // [rows, ld_out]
     int64_t ld_out;
 };
 
+// B rows of N tile nt: gated: 128 rows of Wg (even CTA) or Wu (odd CTA);
+// down: rows [256 nt, 256 nt + 256) of Wd, the odd CTA taking the upper 128.
 template <bool kGated>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, GemmArgs args) {
@@ -86,15 +97,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();     // 0: issues the MMAs
+    const int cluster = (int)blockIdx.x >> 1;
+    const int n_clusters = (int)gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(full_bar(s), 1);     // even CTA's producer + both CTAs' bytes
+            mbar_init(empty_bar(s), 1);    // the pair's MMA commit
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), 128);
+            mbar_init(tempty_bar(b), 8);   // one lane of 4 epilogue warps x 2 CTAs
         }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
@@ -105,46 +119,41 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         prefetch_map(&tmB0);
         if (kGated) prefetch_map(&tmB1);
     }
-    if (warp == 2) {
-        tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
-    }
+    if (warp == 2) tmem_alloc_pair(smem_u32(tmem_holder), TMEM_COLS);
     fence_before();
-    __syncthreads();
+    cluster_sync();   // barriers of both CTAs initialised, TMEM allocated
     fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    const int n_tiles_m = args.hdr_ro->n_fat_tiles;
-    const int total = n_tiles_m * args.n_blocks_n;
-    const int b_tile_rows = kGated ? 128 : 256;
+    const int n_pairs = args.hdr_ro->n_fat_tiles >> 1;
+    const int total = n_pairs * args.n_blocks_n;
 
     if (warp == 0 && lane == 0) {
-        // ---------------- TMA producer ----------------
+        // ---------------- TMA producer (both CTAs) ----------------
+        const CUtensorMap* tmB = (kGated && rank == 1) ? &tmB1 : &tmB0;
+        const uint32_t full0 = mapa_shared(full_bar(0), 0);   // even CTA's barriers
         int stage = 0;
         uint32_t phase = 0;
-        int pending[STAGES];
-        for (int s = 0; s < STAGES; ++s) pending[s] = -1;
+        int rounds[STAGES];
+        for (int s = 0; s < STAGES; ++s) rounds[s] = -1;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-            const int mt = t / args.n_blocks_n;
-            const int nt = t % args.n_blocks_n;
-            const FatTile ft = args.tiles[mt];
-            const int brow = ft.expert * args.b_rows_per_expert + nt * b_tile_rows;
+        for (int w = cluster; ok && w < total; w += n_clusters) {
+            const int pair = w / args.n_blocks_n;
+            const int nt = w % args.n_blocks_n;
+            const FatTile ft = args.tiles[2 * pair + (int)rank];
+            const int brow = ft.expert * args.b_rows_per_expert + nt * (kGated ? BM : BN_MMA) +
+                             (int)rank * args.b_half_rows;
             for (int kb = 0; kb < args.k_blocks; ++kb) {
                 if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
                     ok = false;
                     break;
                 }
                 const uint32_t sa = base + stage * STAGE_BYTES;
-                const uint32_t sb = sa + A_BYTES;
-                mbar_expect_tx(full_bar(stage), STAGE_BYTES);
-                tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, ft.row0);
-                if (kGated) {
-                    tma_load_2d(sb, &tmB0, full_bar(stage), kb * BK, brow);
-                    tma_load_2d(sb + B_BYTES / 2, &tmB1, full_bar(stage), kb * BK, brow);
-                } else {
-                    tma_load_2d(sb, &tmB0, full_bar(stage), kb * BK, brow);
-                }
-                pending[stage] = (int)phase;
+                const uint32_t fb = full0 + 8u * stage;
+                if (rank == 0) mbar_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
+                tma_load_2d_pair(sa, &tmA, fb, kb * BK, ft.row0);
+                tma_load_2d_pair(sa + A_BYTES, tmB, fb, kb * BK, brow);
+                rounds[stage] = (int)phase;
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
@@ -154,18 +163,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         if (!ok) {
             *abort_flag = 1;
             set_status(args.hdr, MOE_ERR_TIMEOUT);
-            // Let the copies already issued land before the CTA exits.
-            for (int s = 0; s < STAGES; ++s)
-                if (pending[s] >= 0) (void)mbar_wait(full_bar(s), (uint32_t)pending[s]);
         }
-    } else if (warp == 1 && lane == 0) {
-        // ---------------- MMA issuer ----------------
+        // Tail: every stage this CTA filled has been read by the pair's MMAs
+        // (its copies have landed) before the CTA may leave.
+        for (int s = 0; s < STAGES; ++s)
+            if (rounds[s] >= 0) (void)mbar_wait(empty_bar(s), (uint32_t)rounds[s]);
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ---------------- MMA issuer (even CTA) ----------------
         int stage = 0;
         uint32_t phase = 0;
         int it = 0;
         bool ok = true;
         bool issued = false;
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++it) {
+        for (int w = cluster; ok && w < total; w += n_clusters, ++it) {
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)((it >> 1) & 1);
             if (*abort_flag || !mbar_wait(tempty_bar(acc), acc_phase ^ 1u)) {
@@ -181,40 +191,40 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 }
                 fence_after();
                 const uint32_t sa = base + stage * STAGE_BYTES;
-                const uint32_t sb = sa + A_BYTES;
                 const uint64_t ad = sw128_desc(sa);
-                const uint64_t bd = sw128_desc(sb);
+                const uint64_t bd = sw128_desc(sa + A_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     // +32 bytes per 16-element K step inside the swizzle row
-                    mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), kIdesc,
-                             (kb > 0 || kk > 0) ? 1u : 0u);
+                    mma_bf16_pair(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
+                                  kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
                 }
                 issued = true;
-                commit(empty_bar(stage));
+                commit_pair_multicast(empty_bar(stage), kPairMask);
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) break;
-            commit(tfull_bar(acc));
+            commit_pair_multicast(tfull_bar(acc), kPairMask);
         }
         if (!ok) {
             *abort_flag = 1;
             set_status(args.hdr, MOE_ERR_TIMEOUT);
             if (issued) {
                 // Wait for every MMA issued so far before TMEM is freed.
-                commit(done_bar);
+                commit_pair_multicast(done_bar, 0x1);
                 (void)mbar_wait(done_bar, 0);
             }
         }
     } else if (warp >= 4) {
-        // ---------------- epilogue ----------------
+        // ---------------- epilogue (both CTAs) ----------------
         const int ew = warp - 4;              // TMEM lanes 32*ew .. 32*ew+31
         const int row = ew * 32 + lane;
+        const uint32_t tempty0 = mapa_shared(tempty_bar(0), 0);
         int it = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+        for (int w = cluster; w < total; w += n_clusters, ++it) {
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)((it >> 1) & 1);
             if (*abort_flag || !mbar_wait(tfull_bar(acc), acc_phase)) {
@@ -223,9 +233,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 break;
             }
             fence_after();
-            const int mt = t / args.n_blocks_n;
-            const int nt = t % args.n_blocks_n;
-            const FatTile ft = args.tiles[mt];
+            const int pair = w / args.n_blocks_n;
+            const int nt = w % args.n_blocks_n;
+            const FatTile ft = args.tiles[2 * pair + (int)rank];
             const bool valid = row < ft.rows;
             __nv_bfloat16* dst = args.out + (int64_t)(ft.row0 + row) * args.ld_out +
                                  (int64_t)nt * args.bn_out;
@@ -272,15 +282,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 }
             }
             fence_before();
-            mbar_arrive(tempty_bar(acc));
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * acc);
         }
     }
 
     fence_before();
     __syncthreads();
+    cluster_sync();   // the pair is done with each other's barriers and TMEM
     if (warp == 2) {
         fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 
@@ -316,6 +328,33 @@ cudaError_t set_smem_attr() {
     return err;
 }
 
+// CTAs to launch: two per co-resident cluster (an SM pair whose partner is
+// busy or absent cannot host a cluster, so this can be below the SM count).
+template <bool kGated>
+cudaError_t pair_grid(int num_sms, int* grid) {
+    constexpr int kMaxDev = 64;
+    static int cached[kMaxDev] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    if (!cached[dev]) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(num_sms & ~1), 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.dynamicSmemBytes = SMEM_BYTES;
+        int clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<kGated>, &cfg);
+        if (e != cudaSuccess) return e;
+        if (clusters < 1) return cudaErrorInvalidConfiguration;
+        cached[dev] = 2 * std::min(clusters, num_sms / 2);
+    }
+    *grid = cached[dev];
+    return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t make_tma_map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
@@ -342,6 +381,8 @@ cudaError_t launch_gemm_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_allo
     if ((e = make_tma_map_bf16(&mG, Wg, (uint64_t)E * I, (uint64_t)H, 128)) != cudaSuccess) return e;
     if ((e = make_tma_map_bf16(&mU, Wu, (uint64_t)E * I, (uint64_t)H, 128)) != cudaSuccess) return e;
     if ((e = set_smem_attr<true>()) != cudaSuccess) return e;
+    int grid = 0;
+    if ((e = pair_grid<true>(num_sms, &grid)) != cudaSuccess) return e;
     GemmArgs a;
     a.tiles = plan.tiles;
     a.hdr_ro = plan.hdr;
@@ -349,10 +390,11 @@ cudaError_t launch_gemm_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_allo
     a.n_blocks_n = I / 128;
     a.k_blocks = H / BK;
     a.b_rows_per_expert = I;
+    a.b_half_rows = 0;        // the odd CTA reads the same rows of Wu
     a.bn_out = 128;
     a.out = h;
     a.ld_out = I;
-    grouped_gemm_kernel<true><<<num_sms, 256, SMEM_BYTES, s>>>(mA, mG, mU, a);
+    grouped_gemm_kernel<true><<<grid, 256, SMEM_BYTES, s>>>(mA, mG, mU, a);
     return cudaGetLastError();
 }
 
@@ -363,8 +405,10 @@ cudaError_t launch_gemm_down(const __nv_bfloat16* h, int64_t rows_alloc,
     CUtensorMap mA, mD;
     cudaError_t e;
     if ((e = make_tma_map_bf16(&mA, h, (uint64_t)rows_alloc, (uint64_t)I, BM)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16(&mD, Wd, (uint64_t)E * H, (uint64_t)I, 256)) != cudaSuccess) return e;
+    if ((e = make_tma_map_bf16(&mD, Wd, (uint64_t)E * H, (uint64_t)I, 128)) != cudaSuccess) return e;
     if ((e = set_smem_attr<false>()) != cudaSuccess) return e;
+    int grid = 0;
+    if ((e = pair_grid<false>(num_sms, &grid)) != cudaSuccess) return e;
     GemmArgs a;
     a.tiles = plan.tiles;
     a.hdr_ro = plan.hdr;
@@ -372,10 +416,11 @@ cudaError_t launch_gemm_down(const __nv_bfloat16* h, int64_t rows_alloc,
     a.n_blocks_n = H / 256;
     a.k_blocks = I / BK;
     a.b_rows_per_expert = H;
+    a.b_half_rows = 128;      // the odd CTA reads the upper half of the 256 rows
     a.bn_out = 256;
     a.out = y_sorted;
     a.ld_out = H;
-    grouped_gemm_kernel<false><<<num_sms, 256, SMEM_BYTES, s>>>(mA, mD, mD, a);
+    grouped_gemm_kernel<false><<<grid, 256, SMEM_BYTES, s>>>(mA, mD, mD, a);
     return cudaGetLastError();
 }
 

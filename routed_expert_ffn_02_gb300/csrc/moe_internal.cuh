@@ -31,7 +31,7 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 // One grouped-GEMM row tile: rows [row0, row0 + rows) of expert `expert`
-// in sorted-slot order.
+// in sorted-slot order (rows may be 0 for the second tile of a pair).
 struct FatTile {
     int32_t expert;
     int32_t row0;
@@ -76,7 +76,8 @@ struct Plan {
 // (<= 256 items) is faster on CUDA cores, batch 4 (<= 512) on tensor cores.
 constexpr int kThinMmaAutoItems = 384;
 
-inline int64_t max_fat_tiles(int64_t P, int E) { return P / kTileM + E + 1; }
+// Fat tiles come in pairs per expert: sum_e 2*ceil(c_e/256) <= P/128 + 2E.
+inline int64_t max_fat_tiles(int64_t P, int E) { return P / kTileM + 2 * (int64_t)E + 2; }
 inline int64_t max_thin_units(int E, int unit_tokens) {
     return (int64_t)E * ((kThinMaxTokens + unit_tokens - 1) / unit_tokens);
 }
@@ -139,6 +140,9 @@ cudaError_t launch_gemm_down(const __nv_bfloat16* h, int64_t rows_alloc,
 cudaError_t launch_combine(const __nv_bfloat16* y_sorted, const int32_t* inv_perm,
                            const float* gates, int T, int k, int H,
                            __nv_bfloat16* out, int num_sms, cudaStream_t s);
+
+// Validates a moe_shape as every entry point does (sets moe_last_error()).
+moe_status check_shape_status(const moe_shape* shape);
 
 // Sets the calling thread's moe_last_error() message (printf format).
 void set_last_error(const char* fmt, ...);

@@ -67,8 +67,8 @@ __device__ int block_exclusive_scan(int* a, int n, int* ws) {
     return total;
 }
 
-// Planner: fat experts (count >= threshold, count > 0) get ceil(count/128)
-// row tiles; thin experts (0 < count < threshold) with at least thin_mma_min
+// Planner: fat experts (count >= threshold, count > 0) get 2*ceil(count/256)
+// row tiles of up to 128 rows; thin experts (0 < count < threshold) with at least thin_mma_min
 // slots get one tile for the tensor-core streaming kernel; the other thin
 // experts get ceil(count/unit_tokens) CUDA-core streaming units, each with the
 // running sum of unit costs before it (thin_unit_cost) so that kernel can
@@ -83,9 +83,13 @@ __device__ void block_plan(const int* cnt, const int* off, int E, const Plan& pl
     auto is_fat = [&](int c) { return c > 0 && c >= thr; };
     auto is_mma = [&](int c) { return c > 0 && c < thr && c >= mma_min; };
     auto is_unit = [&](int c) { return c > 0 && c < thr && c < mma_min; };
+    // A fat expert's 128-row tiles come in pairs (a 256-row block of its
+    // slots: tiles 2q and 2q+1 cover rows [256q, 256q+128) and
+    // [256q+128, 256q+256)), so the grouped GEMM can run each pair on a CTA
+    // pair; the second tile of a ragged block may hold 0 rows.
     for (int e = threadIdx.x; e < E; e += NT) {
         const int c = cnt[e];
-        ta[e] = is_fat(c) ? (c + kTileM - 1) / kTileM : 0;
+        ta[e] = is_fat(c) ? 2 * ((c + 2 * kTileM - 1) / (2 * kTileM)) : 0;
         tb[e] = is_mma(c) ? 1 : 0;
     }
     __syncthreads();
@@ -94,12 +98,12 @@ __device__ void block_plan(const int* cnt, const int* off, int E, const Plan& pl
     for (int e = threadIdx.x; e < E; e += NT) {
         const int c = cnt[e];
         if (is_fat(c)) {
-            const int nt = (c + kTileM - 1) / kTileM;
+            const int nt = 2 * ((c + 2 * kTileM - 1) / (2 * kTileM));
             for (int i = 0; i < nt; ++i) {
                 FatTile ft;
                 ft.expert = e;
                 ft.row0 = off[e] + i * kTileM;
-                ft.rows = min(kTileM, c - i * kTileM);
+                ft.rows = max(0, min(kTileM, c - i * kTileM));
                 ft.pad = 0;
                 plan.tiles[ta[e] + i] = ft;
             }

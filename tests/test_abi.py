@@ -148,3 +148,24 @@ def test_forward_launch_count(moe):
     assert moe.forward_launches(S(16384, 384, 8, 4096, 2048, thin_mma_min=8)) == 12
     assert moe.forward_launches(S(16384, 384, 8, 4096, 2048, fat_threshold=0)) == 8
     assert moe.forward_launches(S(0, 384, 8, 4096, 2048)) == 0
+
+
+def test_pipe_argument_errors(moe):
+    """moe_forward_host rejects a NULL pipe, equal streams and a small
+    workspace before touching the GPU; the pipe workspace adds two staging
+    slots to the forward workspace."""
+    lib = moe.binding.raw_lib()
+    shape = moe.binding.MoeShape(16, 16, 2, 512, 256, 32)
+    fwd = lib.moe_workspace_size(ctypes.byref(shape))
+    slot = 16 * 512 * 2 + 16 * 16 * 4 + 16 * 512 * 2   # x, logits, out (each 256-aligned here)
+    assert lib.moe_pipe_workspace_size(ctypes.byref(shape)) == fwd + 2 * slot
+    bad = moe.binding.MoeShape(16, 16, 2, 100, 256, 32)
+    assert lib.moe_pipe_workspace_size(ctypes.byref(bad)) == 0
+    s1, s2, s3 = ctypes.c_void_p(1), ctypes.c_void_p(2), ctypes.c_void_p(3)
+    args = [None] * 7 + [0]          # logits, x, 3 weights, out, ws, ws_bytes
+    assert lib.moe_forward_host(None, ctypes.byref(shape), *args, s1, s2, s3) == 1
+    fake = ctypes.c_void_p(8)   # never dereferenced: the stream check comes first
+    assert lib.moe_forward_host(fake, ctypes.byref(shape), *args, s1, s1, s3) == 1
+    assert b"different streams" in lib.moe_last_error()
+    assert lib.moe_forward_host(fake, ctypes.byref(bad), *args, s1, s2, s3) == 1
+    assert lib.moe_pipe_create(None) == 1
