@@ -236,20 +236,29 @@ size_t moe_layer_weight_bytes(const moe_shape* shape);
 
 /* Creates a stager over caller-owned device memory `slots` (n_slots slots of
  * slot_bytes each, 256-byte aligned, slot_bytes a multiple of 256).  The
- * stager allocates no device memory; it owns two CUDA events per slot.  The
- * slots must outlive the stager and every forward enqueued with it. */
+ * stager allocates no device memory; it owns two CUDA events per slot and a
+ * pinned host flag array (n_layers x E bytes, allocated by the first forward
+ * that needs it).  The slots must outlive the stager and every forward
+ * enqueued with it. */
 moe_status moe_stager_create(void* slots, int32_t n_slots, size_t slot_bytes,
                              moe_stager** out);
 moe_status moe_stager_destroy(moe_stager* stager);
 
-/* Runs n_layers independent layers on the same activations x [T, H] (device):
- * for layer l, host_weights[l] (pinned host memory, moe_layer_weight_bytes
- * bytes, W_gate | W_up | W_down) is copied into slot l mod n_slots on `copy`
- * once the compute that last used that slot has finished, and moe_forward
- * runs on `compute` once the copy has landed, with logits[l] [T, E] and
- * out[l] [T, H] (device).  All copies are enqueued up front, so the copy
- * engine works up to n_slots layers ahead.  `copy` must differ from
- * `compute`; ws as for moe_forward.  Asynchronous; errors as moe_forward. */
+/* Runs n_layers independent layers on the same activations x [T, H] (device)
+ * with logits[l] [T, E] and out[l] [T, H] (device), expert weights in
+ * host_weights[l] (pinned host memory, moe_layer_weight_bytes bytes,
+ * W_gate | W_up | W_down).  First every layer is routed on `compute` and the
+ * experts it touches are marked in a pinned flag array owned by the stager;
+ * the call synchronises `compute` once to read them (wiki file map: only
+ * experts with positive counts are copied).  Then, for layer l, each run of
+ * consecutive touched experts of each matrix is copied into the same offsets
+ * of slot l mod n_slots on `copy`, once the compute that last used that slot
+ * has finished, and moe_forward runs on `compute` once the copies have
+ * landed; untouched experts' regions of the slot are neither copied nor
+ * read.  All copies are enqueued up front, so the copy engine works up to
+ * n_slots layers ahead.  `copy` must differ from `compute`; ws as for
+ * moe_forward.  Errors as moe_forward, plus MOE_ERR_CUDA if the flag array
+ * cannot be allocated. */
 moe_status moe_forward_offload(moe_stager* stager, const moe_shape* shape, int32_t n_layers,
                                const float* const* logits, const moe_bf16* x,
                                const void* const* host_weights, moe_bf16* const* out,

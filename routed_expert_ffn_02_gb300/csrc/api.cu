@@ -114,6 +114,7 @@ moe_status check_shape(const moe_shape* sh) {
 
 moe_status moe::check_shape_status(const moe_shape* shape) { return check_shape(shape); }
 
+
 namespace {
 
 int thin_mma_min(const moe_shape* sh) {
@@ -287,6 +288,21 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
 }
 
 }  // namespace
+
+moe_status moe::mark_touched_experts(const moe_shape* shape, const float* logits, void* ws,
+                                     size_t ws_bytes, uint8_t* flags, cudaStream_t s) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    if (shape->T == 0) return MOE_OK;
+    if (!logits || !flags) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+    FwdBufs b;
+    if ((st = check_ws(ws, ws_bytes, carve_fwd(shape, nullptr, &b))) != MOE_OK) return st;
+    carve_fwd(shape, ws, &b);
+    CUDA_TRY(launch_route(logits, shape->T, shape->E, shape->k, b.idx, b.gates, s), "route");
+    CUDA_TRY(launch_mark_touched(b.idx, (int64_t)shape->T * shape->k, shape->E, flags, s),
+             "mark touched experts");
+    return MOE_OK;
+}
 
 extern "C" {
 

@@ -89,6 +89,11 @@ int thin_unit_tokens(int H, int I);
 cudaError_t launch_route(const float* logits, int T, int E, int k,
                          int32_t* idx, float* gates, cudaStream_t s);
 
+// flags[e] = 1 for every expert e in idx[0, P) (flags: device-visible memory,
+// e.g. mapped pinned host memory; never cleared here).
+cudaError_t launch_mark_touched(const int32_t* idx, int64_t P, int E, uint8_t* flags,
+                                cudaStream_t s);
+
 // Route lists; when plan != nullptr the planner runs in the same kernels.
 cudaError_t launch_permute(const int32_t* idx, int T, int E, int k,
                            int32_t* counts, int32_t* offsets, int32_t* perm,
@@ -140,6 +145,11 @@ cudaError_t launch_gemm_down(const __nv_bfloat16* h, int64_t rows_alloc,
 cudaError_t launch_combine(const __nv_bfloat16* y_sorted, const int32_t* inv_perm,
                            const float* gates, int T, int k, int H,
                            __nv_bfloat16* out, int num_sms, cudaStream_t s);
+
+// Routes `logits` into the routing buffers of a moe_forward workspace and
+// sets flags[e] = 1 for each expert the layer touches (asynchronous on s).
+moe_status mark_touched_experts(const moe_shape* shape, const float* logits, void* ws,
+                                size_t ws_bytes, uint8_t* flags, cudaStream_t s);
 
 // Validates a moe_shape as every entry point does (sets moe_last_error()).
 moe_status check_shape_status(const moe_shape* shape);

@@ -12,6 +12,8 @@
 // next expert to select; k rounds of a warp max-reduction pick the top k in
 // output order.  Key 0 marks an empty or already-taken candidate and sorts
 // below every real logit, including -inf.
+#include <algorithm>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -97,7 +99,26 @@ cudaError_t launch_epl(const float* logits, int T, int E, int k, int32_t* idx,
     return cudaGetLastError();
 }
 
+// flags[idx[s]] = 1 for every routed slot (every writer stores the same
+// value, so the races are benign); indices outside [0, E) are skipped.
+__global__ void __launch_bounds__(256)
+mark_touched_kernel(const int32_t* __restrict__ idx, int64_t P, int E, uint8_t* flags) {
+    for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < P;
+         s += (int64_t)gridDim.x * blockDim.x) {
+        const int e = idx[s];
+        if ((unsigned)e < (unsigned)E) flags[e] = 1;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_mark_touched(const int32_t* idx, int64_t P, int E, uint8_t* flags,
+                                cudaStream_t s) {
+    if (P == 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>((P + 255) / 256, 1024);
+    mark_touched_kernel<<<(int)blocks, 256, 0, s>>>(idx, P, E, flags);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_route(const float* logits, int T, int E, int k,
                          int32_t* idx, float* gates, cudaStream_t s) {

@@ -5,18 +5,28 @@
 // of device staging slots in batches by the copy engine, overlapped with
 // compute, with the next layers' copies issued while the current layer runs
 // (dsv41-flash-offload wiki, overview and its notes on 8 staging slots and
-// cross-layer DMA prefetch).  Here one slot holds one layer's whole expert set
-// (W_gate | W_up | W_down, the layout moe_forward takes), which a 16k-token
-// chunk touches almost entirely.  For layer l (slot s = l mod n_slots):
+// cross-layer DMA prefetch).  Here one slot has room for one layer's whole
+// expert set (W_gate | W_up | W_down, the layout moe_forward takes), but only
+// the experts the layer's tokens are routed to are copied (the wiki's file
+// map: one weight copy per batch for the experts with positive counts).
 //
-//   copy stream:    wait for the compute that last used slot s (layer l - n),
-//                   cudaMemcpyAsync host_weights[l] -> slot s, record copied[s]
-//   compute stream: wait copied[s], moe_forward on the slot, record freed[s]
+//   1. compute stream: route every layer and mark its touched experts in a
+//      pinned host flag array (written by the GPU); synchronise once.
+//   2. for layer l (slot s = l mod n_slots):
+//      copy stream:    wait for the compute that last used slot s (layer
+//                      l - n), one cudaMemcpyAsync per matrix per run of
+//                      consecutive touched experts into the same offsets of
+//                      slot s, record copied[s]
+//      compute stream: wait copied[s], moe_forward on the slot, record
+//                      freed[s]
 //
-// Every copy for all layers is enqueued up front, so the copy engine runs up
-// to n_slots layers ahead of the compute.  The caller owns the slot memory;
-// the stager holds only its events.
+// Untouched experts' regions of a slot keep stale bytes and are never read:
+// no token is routed to them.  Every copy for all layers is enqueued up front,
+// so the copy engine runs up to n_slots layers ahead of the compute.  The
+// caller owns the slot memory; the stager holds its events and the flag
+// array (pinned host memory, grown on demand).
 #include <cstdlib>
+#include <cstring>
 #include <new>
 
 #include "moe_internal.cuh"
@@ -27,6 +37,9 @@ struct moe_stager {
     size_t slot_bytes;
     cudaEvent_t* copied;
     cudaEvent_t* freed;
+    uint8_t* flags_h;      // [n_layers x E] touched flags, pinned and mapped
+    uint8_t* flags_d;      // the device's view of flags_h
+    size_t flags_cap;
 };
 
 namespace {
@@ -51,6 +64,9 @@ extern "C" moe_status moe_stager_create(void* slots, int32_t n_slots, size_t slo
     st->slots = static_cast<uint8_t*>(slots);
     st->n_slots = n_slots;
     st->slot_bytes = slot_bytes;
+    st->flags_h = nullptr;
+    st->flags_d = nullptr;
+    st->flags_cap = 0;
     st->copied = new (std::nothrow) cudaEvent_t[n_slots]();
     st->freed = new (std::nothrow) cudaEvent_t[n_slots]();
     if (!st->copied || !st->freed) {
@@ -85,6 +101,7 @@ extern "C" moe_status moe_stager_destroy(moe_stager* st) {
     }
     delete[] st->copied;
     delete[] st->freed;
+    if (st->flags_h) cudaFreeHost(st->flags_h);
     delete st;
     return MOE_OK;
 }
@@ -110,17 +127,70 @@ extern "C" moe_status moe_forward_offload(moe_stager* st, const moe_shape* shape
         return stager_fail(MOE_ERR_INVALID_ARG,
                            "moe_forward_offload: the copy stream must differ from the compute stream");
     cudaStream_t cs = (cudaStream_t)compute, ks = (cudaStream_t)copy;
-    const size_t per = (size_t)shape->E * shape->I * shape->H;   // elements per matrix
+    const int E = shape->E;
+    const size_t per = (size_t)E * shape->I * shape->H;            // elements per matrix
+    const size_t per_expert = (size_t)shape->I * shape->H * sizeof(moe_bf16);
+    for (int l = 0; l < n_layers; ++l)
+        if (!host_weights[l] || !logits[l] || !out[l])
+            return stager_fail(MOE_ERR_INVALID_ARG, "moe_forward_offload: NULL layer pointer");
+    if (n_layers == 0 || shape->T == 0) {
+        moe::set_last_error("");
+        return MOE_OK;
+    }
+    cudaError_t e = cudaSuccess;
+    // 1. touched experts of every layer, written by the GPU into pinned
+    // host flags (the previous call's readers are done: it synchronised).
+    const size_t need = (size_t)n_layers * E;
+    if (need > st->flags_cap) {
+        if (st->flags_h) cudaFreeHost(st->flags_h);
+        st->flags_h = nullptr;
+        st->flags_d = nullptr;
+        st->flags_cap = 0;
+        void* h = nullptr;
+        void* d = nullptr;
+        if ((e = cudaHostAlloc(&h, need, cudaHostAllocMapped)) != cudaSuccess ||
+            (e = cudaHostGetDevicePointer(&d, h, 0)) != cudaSuccess) {
+            if (h) cudaFreeHost(h);
+            moe::set_last_error("moe_forward_offload: %s", cudaGetErrorString(e));
+            return MOE_ERR_CUDA;
+        }
+        st->flags_h = static_cast<uint8_t*>(h);
+        st->flags_d = static_cast<uint8_t*>(d);
+        st->flags_cap = need;
+    }
+    memset(st->flags_h, 0, need);
+    for (int l = 0; l < n_layers; ++l) {
+        const moe_status ms = moe::mark_touched_experts(shape, logits[l], ws, ws_bytes,
+                                                        st->flags_d + (size_t)l * E, cs);
+        if (ms != MOE_OK) return ms;
+    }
+    if ((e = cudaStreamSynchronize(cs)) != cudaSuccess) {
+        moe::set_last_error("moe_forward_offload: %s", cudaGetErrorString(e));
+        return MOE_ERR_CUDA;
+    }
+    // 2. copies of the touched experts and the layers' compute.
     for (int l = 0; l < n_layers; ++l) {
         const int s = l % st->n_slots;
         uint8_t* slot = st->slots + (size_t)s * st->slot_bytes;
-        if (!host_weights[l] || !logits[l] || !out[l])
-            return stager_fail(MOE_ERR_INVALID_ARG, "moe_forward_offload: NULL layer pointer");
-        cudaError_t e = cudaSuccess;
+        const uint8_t* src = static_cast<const uint8_t*>(host_weights[l]);
+        const uint8_t* touched = st->flags_h + (size_t)l * E;
         // The slot may be refilled only once the compute of its last layer
         // has finished (that event was recorded in an earlier iteration).
         if (l >= st->n_slots) e = cudaStreamWaitEvent(ks, st->freed[s], 0);
-        if (e == cudaSuccess) e = cudaMemcpyAsync(slot, host_weights[l], wbytes, cudaMemcpyHostToDevice, ks);
+        for (int e0 = 0; e == cudaSuccess && e0 < E;) {
+            if (!touched[e0]) {
+                ++e0;
+                continue;
+            }
+            int e1 = e0 + 1;
+            while (e1 < E && touched[e1]) ++e1;
+            const size_t off = (size_t)e0 * per_expert, len = (size_t)(e1 - e0) * per_expert;
+            for (int m = 0; e == cudaSuccess && m < 3; ++m) {
+                const size_t mo = (size_t)m * per * sizeof(moe_bf16) + off;
+                e = cudaMemcpyAsync(slot + mo, src + mo, len, cudaMemcpyHostToDevice, ks);
+            }
+            e0 = e1;
+        }
         if (e == cudaSuccess) e = cudaEventRecord(st->copied[s], ks);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, st->copied[s], 0);
         if (e != cudaSuccess) {

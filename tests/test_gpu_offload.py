@@ -43,6 +43,33 @@ def test_offload_matches_resident_forward(moe, T, E, k, H, I, L, slots):
     st.close()
 
 
+@pytest.mark.parametrize("T,E,k,H,I,L,slots", [(4, 64, 8, 512, 256, 3, 2),
+                                                (512, 48, 4, 1024, 512, 4, 3)])
+def test_offload_copies_exactly_the_touched_experts(moe, T, E, k, H, I, L, slots):
+    """Slots are filled with NaN before the forward: only the experts a
+    layer's tokens are routed to are copied, and nothing else is read, so the
+    outputs still equal the resident forward (and hold no NaN)."""
+    shape = moe.Shape(T, E, k, H, I)
+    dev = torch.device("cuda")
+    x = synth.make_x(T, H, seed=1).to(dev)
+    logits = [synth.make_logits(T, E, seed=1, layer=l, zipf_s=synth.ZIPF_S).to(dev) for l in range(L)]
+    weights = [synth.make_weights(E, H, I, seed=1, layer=l, device=dev) for l in range(L)]
+    host = [moe.pack_layer_weights(*w) for w in weights]
+    st = moe.Stager(shape, slots)
+    st.slots.view(torch.int16).fill_(0x7FC0)        # bf16 quiet NaN
+    torch.cuda.synchronize()
+    outs = st.forward(shape, logits, x, host)
+    torch.cuda.synchronize()
+    touched = [torch.unique(moe.moe_route(lg, k)[0]).numel() for lg in logits]
+    assert min(touched) < E                         # some experts are never copied
+    for l in range(L):
+        ref = moe.moe_forward(shape, logits[l], x, *weights[l])
+        torch.cuda.synchronize()
+        assert torch.isfinite(outs[l].float()).all(), f"layer {l}"
+        assert torch.equal(outs[l], ref), f"layer {l}"
+    st.close()
+
+
 def test_offload_argument_errors(moe):
     shape = moe.Shape(8, 16, 2, 512, 256)
     small = moe.Shape(8, 8, 2, 512, 256)
