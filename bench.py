@@ -142,13 +142,17 @@ def stage_work(shape, counts_np):
     thin = (counts_np > 0) & (counts_np < thr)
     fat_rows = int(counts_np[fat].sum())
     thin_rows = int(counts_np[thin].sum())
+    # x_sorted holds the rows of fat experts and of thin experts on the
+    # tensor-core streaming kernel (the library's rule when thin_mma_min is 0)
+    mma_min = shape.thin_mma_min or (1 if min(E, P) * (I // 128) >= 384 else 33)
+    mma_rows = int(counts_np[thin & (counts_np >= mma_min)].sum())
     n_fat, n_thin = int(fat.sum()), int(thin.sum())
     w_gu = 2 * I * H * 2      # gate + up bytes per expert
     w_d = H * I * 2
     return {
         "route": dict(bytes=T * E * 4 + P * 8, flops=0),
         "permute": dict(bytes=P * 4 * 4 + E * 8, flops=0),
-        "gather": dict(bytes=fat_rows * H * 2 * 2, flops=0),
+        "gather": dict(bytes=(fat_rows + mma_rows) * H * 2 * 2, flops=0),
         "gemm_gate_up": dict(flops=2 * fat_rows * H * 2 * I,
                              bytes=n_fat * w_gu + fat_rows * (H + I) * 2),
         "thin_gate_up": dict(bytes=n_thin * w_gu + thin_rows * (H + I) * 2,
@@ -240,19 +244,17 @@ def time_steps(layer, steps, warmup, profiled=True, rotate=True):
 
 
 def time_graph_steps(layer, steps, warmup, n_graphs=8):
-    """Times `steps` forwards replayed from CUDA graphs (one graph per logits
-    set, captured once); returns total ms."""
-    stream = torch.cuda.Stream()
+    """Times `steps` decode steps replayed through the library's DecodeGraph
+    (one captured step per logits set, its static inputs filled once);
+    returns total ms."""
+    moe = layer.moe
     graphs = []
-    with torch.cuda.stream(stream):
-        for i in range(n_graphs):
-            layer.forward(i)                      # warm the launch path first
-        torch.cuda.synchronize()
-        for i in range(n_graphs):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                layer.forward(i)
-            graphs.append(g)
+    for i in range(n_graphs):
+        g = moe.DecodeGraph(layer.shape, layer.Wg, layer.Wu, layer.Wd)
+        g.logits.copy_(layer.logits[i % len(layer.logits)])
+        g.x.copy_(layer.x)
+        graphs.append(g)
+    torch.cuda.synchronize()
     for i in range(warmup):
         graphs[i % n_graphs].replay()
     start = torch.cuda.Event(enable_timing=True)
@@ -265,6 +267,8 @@ def time_graph_steps(layer, steps, warmup, n_graphs=8):
     end.record()
     torch.cuda.synchronize()
     barrier()
+    for g in graphs:
+        assert g.ws.status() == 0
     return start.elapsed_time(end)
 
 

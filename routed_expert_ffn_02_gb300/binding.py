@@ -395,6 +395,42 @@ class Pipe:
         self.d2h.synchronize()
 
 
+class DecodeGraph:
+    """moe_forward for one fixed shape (a decode batch) captured once in a
+    CUDA graph, as a serving engine runs decode steps: write the step's
+    inputs into the static buffers `logits` [T, E] fp32 and `x` [T, H] bf16
+    (device), call replay(), read `out` [T, H].  The weights are captured by
+    address and must stay allocated."""
+
+    def __init__(self, shape: Shape, W_gate, W_up, W_down, device=None):
+        device = device or W_gate.device
+        self.shape = shape
+        self.logits = torch.zeros((shape.T, shape.E), dtype=torch.float32, device=device)
+        self.x = torch.zeros((shape.T, shape.H), dtype=torch.bfloat16, device=device)
+        self.out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=device)
+        self.topk_idx = torch.empty((shape.T, shape.k), dtype=torch.int32, device=device)
+        self.gates = torch.empty((shape.T, shape.k), dtype=torch.float32, device=device)
+        self._W = (W_gate, W_up, W_down)
+        self.stream = torch.cuda.Stream(device=device)
+        self.ws = Workspace(workspace_size(shape), device, self.stream)
+        self.stream.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(self.stream):
+            self._forward()                     # resolves lazy state before capture
+        self.stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            self._forward()
+
+    def _forward(self):
+        moe_forward(self.shape, self.logits, self.x, *self._W, out=self.out,
+                    topk_idx=self.topk_idx, gates=self.gates, ws=self.ws, stream=self.stream)
+
+    def replay(self):
+        """Runs the captured layer on the current stream's timeline."""
+        self.graph.replay()
+        return self.out
+
+
 def raw_lib():
     """The loaded ctypes library (for callers that pass raw pointers)."""
     return _lib
