@@ -10,6 +10,8 @@
 
 using namespace moe;
 
+thread_local bool moe::t_pdl = false;
+
 namespace {
 
 thread_local char g_err[512] = "";
@@ -370,6 +372,7 @@ moe_status moe_expert_ffn(const moe_shape* shape, const moe_bf16* x, const int32
     if ((st = device_info(&dev)) != MOE_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     const Plan plan = make_plan(shape, b.tiles, b.units, b.mma_tiles, b.hdr);
+    const PdlScope pdl((int64_t)shape->T * shape->k <= kPermChunk);
     CUDA_TRY(launch_plan(counts, offsets, shape->E, plan, s), "plan");
     st = run_experts(shape, dev, (const __nv_bfloat16*)x, perm, offsets, counts,
                      (const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
@@ -418,6 +421,7 @@ static moe_status forward_impl(const moe_shape* shape, const float* logits, cons
     if ((st = device_info(&dev)) != MOE_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     const int T = shape->T, E = shape->E, k = shape->k;
+    const PdlScope pdl((int64_t)T * k <= kPermChunk);
     int32_t* idx = topk_idx ? topk_idx : b.idx;
     float* g = gates ? gates : b.gates;
     CUDA_TRY(mark(ev, kEvStart, s), "cudaEventRecord");

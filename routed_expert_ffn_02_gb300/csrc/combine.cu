@@ -4,6 +4,7 @@
 // fp32 accumulation in ascending j, no atomics, so repeated runs are
 // bit-identical.  One block per token row (grid-stride), 16-byte vectors.
 #include "moe_internal.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -12,6 +13,8 @@ __global__ void __launch_bounds__(256)
 combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ inv_perm,
                const float* __restrict__ gates, int T, int k, int H,
                uint4* __restrict__ out) {
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
     const int vec = H / 8;
     for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
         int64_t src[kMaxK];
@@ -54,10 +57,9 @@ cudaError_t launch_combine(const __nv_bfloat16* y_sorted, const int32_t* inv_per
                            __nv_bfloat16* out, int num_sms, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const int blocks = (int)std::min<int64_t>(T, (int64_t)num_sms * 8);
-    combine_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(y_sorted),
-                                          inv_perm, gates, T, k, H,
-                                          reinterpret_cast<uint4*>(out));
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, s,
+                      reinterpret_cast<const uint4*>(y_sorted), inv_perm, gates, T, k, H,
+                      reinterpret_cast<uint4*>(out));
 }
 
 }  // namespace moe

@@ -128,6 +128,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     cluster_sync();   // barriers of both CTAs initialised, TMEM allocated
     fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    grid_dep_wait();      // everything above overlaps the previous kernel
+    grid_dep_launch();
 
     const int n_pairs = args.hdr_ro->n_fat_tiles >> 1;
     const int total = n_pairs * args.n_blocks_n;
@@ -402,8 +404,8 @@ cudaError_t launch_gemm_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_allo
     a.bn_out = 128;
     a.out = h;
     a.ld_out = I;
-    grouped_gemm_kernel<true><<<grid, 256, SMEM_BYTES, s>>>(mA, mG, mU, a);
-    return cudaGetLastError();
+    return launch_pdl(grouped_gemm_kernel<true>, dim3(grid), dim3(256), SMEM_BYTES, s, mA, mG, mU,
+                      a);
 }
 
 cudaError_t launch_gemm_down(const __nv_bfloat16* h, int64_t rows_alloc,
@@ -428,8 +430,8 @@ cudaError_t launch_gemm_down(const __nv_bfloat16* h, int64_t rows_alloc,
     a.bn_out = 256;
     a.out = y_sorted;
     a.ld_out = H;
-    grouped_gemm_kernel<false><<<grid, 256, SMEM_BYTES, s>>>(mA, mD, mD, a);
-    return cudaGetLastError();
+    return launch_pdl(grouped_gemm_kernel<false>, dim3(grid), dim3(256), SMEM_BYTES, s, mA, mD,
+                      mD, a);
 }
 
 }  // namespace moe

@@ -56,6 +56,37 @@ __host__ __device__ inline int thin_unit_cost(int n) { return (n < 4 ? 4 : n) + 
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Programmatic dependent launch is on for the calling thread's launches while
+// a PdlScope(true) is alive.  The layer entry points turn it on for small
+// batches (decode), where kernel boundaries are a large share of the step;
+// at the prefill chunk, successor CTAs waiting on the SMs cost the GEMMs
+// ~1.5% (measured), so it stays off there.
+extern thread_local bool t_pdl;
+struct PdlScope {
+    bool prev;
+    explicit PdlScope(bool on) : prev(t_pdl) { t_pdl = on; }
+    ~PdlScope() { t_pdl = prev; }
+};
+
+// Launches `kernel` on s, with programmatic stream serialisation when enabled
+// (it may then start while the previous kernel on s finishes; the kernel calls
+// grid_dep_wait() before touching data of earlier kernels).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = t_pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Planner outputs (the split of experts between the expert kernels).  A thin
 // expert (0 < count < fat_threshold) with at least thin_mma_min slots streams
 // its weights through the tensor cores (one FatTile of <= kThinMaxTokens rows

@@ -18,6 +18,7 @@
 //           of one expert is kept.
 // Small inputs (decode) take one single-block kernel doing all of it.
 #include "moe_internal.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -163,6 +164,8 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 __global__ void __launch_bounds__(256)
 hist_kernel(const int32_t* __restrict__ idx, int64_t P, int E,
             int32_t* __restrict__ chunk_hist, WsHeader* hdr) {
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
     __shared__ int h[kMaxE];
     for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
     __syncthreads();
@@ -182,6 +185,8 @@ __global__ void __launch_bounds__(1024)
 scan_kernel(const int32_t* __restrict__ chunk_hist, int nchunks, int E,
             int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts,
             int32_t* __restrict__ offsets, int64_t P, Plan plan, int do_plan) {
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
     __shared__ int cnt[kMaxE], off[kMaxE], ta[kMaxE], tb[kMaxE];
     __shared__ int ws[33];
     const int e = threadIdx.x;
@@ -223,6 +228,8 @@ scatter_kernel(const int32_t* __restrict__ idx, int64_t P, int E,
                const int32_t* __restrict__ chunk_base,
                const int32_t* __restrict__ offsets,
                int32_t* __restrict__ perm, int32_t* __restrict__ inv_perm) {
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
     __shared__ int wc[kScatterWarps][kMaxE];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < kScatterWarps * E; i += blockDim.x)
@@ -275,6 +282,8 @@ permute_small_kernel(const int32_t* __restrict__ idx, int P, int E,
                      int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                      int32_t* __restrict__ perm, int32_t* __restrict__ inv_perm,
                      WsHeader* hdr, Plan plan, int do_plan) {
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
     __shared__ int wc[kScatterWarps][kMaxE];   // reused as planner scratch
     __shared__ int cnt[kMaxE], off[kMaxE];
     __shared__ int ws[33];
@@ -337,6 +346,8 @@ permute_small_kernel(const int32_t* __restrict__ idx, int P, int E,
 __global__ void __launch_bounds__(1024)
 plan_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
             int E, Plan plan) {
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
     __shared__ int cnt[kMaxE], off[kMaxE], ta[kMaxE], tb[kMaxE];
     __shared__ int ws[33];
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -354,6 +365,8 @@ gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
               int k, int H, const FatTile* __restrict__ tiles,
               const FatTile* __restrict__ mma_tiles,
               const WsHeader* __restrict__ hdr, uint4* __restrict__ x_sorted) {
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -389,32 +402,33 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k,
     Plan pl{};
     if (plan) pl = *plan;
     if (P <= kPermChunk) {
-        permute_small_kernel<<<1, 32 * kScatterWarps, 0, s>>>(
-            idx, (int)P, E, counts, offsets, perm, inv_perm, hdr, pl, plan != nullptr);
-        return cudaGetLastError();
+        return launch_pdl(permute_small_kernel, dim3(1), dim3(32 * kScatterWarps), 0, s, idx,
+                          (int)P, E, counts, offsets, perm, inv_perm, hdr, pl,
+                          (int)(plan != nullptr));
     }
     const int nchunks = (int)((P + kPermChunk - 1) / kPermChunk);
-    hist_kernel<<<nchunks, 256, 0, s>>>(idx, P, E, chunk_hist, hdr);
-    scan_kernel<<<1, 1024, 0, s>>>(chunk_hist, nchunks, E, chunk_base, counts,
-                                   offsets, P, pl, plan != nullptr);
-    scatter_kernel<<<nchunks, 32 * kScatterWarps, 0, s>>>(idx, P, E, chunk_base,
-                                                          offsets, perm, inv_perm);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(hist_kernel, dim3(nchunks), dim3(256), 0, s, idx, P, E,
+                               chunk_hist, hdr);
+    if (e == cudaSuccess)
+        e = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, s, chunk_hist, nchunks, E,
+                       chunk_base, counts, offsets, P, pl, (int)(plan != nullptr));
+    if (e == cudaSuccess)
+        e = launch_pdl(scatter_kernel, dim3(nchunks), dim3(32 * kScatterWarps), 0, s, idx, P,
+                       E, chunk_base, offsets, perm, inv_perm);
+    return e;
 }
 
 cudaError_t launch_plan(const int32_t* counts, const int32_t* offsets, int E,
                         const Plan& plan, cudaStream_t s) {
-    plan_kernel<<<1, 1024, 0, s>>>(counts, offsets, E, plan);
-    return cudaGetLastError();
+    return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s, counts, offsets, E, plan);
 }
 
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* perm, int k,
                           int H, const Plan& plan, __nv_bfloat16* x_sorted,
                           int num_sms, cudaStream_t s) {
-    gather_kernel<<<num_sms * 8, 256, 0, s>>>(
-        reinterpret_cast<const uint4*>(x), perm, k, H, plan.tiles, plan.mma_tiles, plan.hdr,
-        reinterpret_cast<uint4*>(x_sorted));
-    return cudaGetLastError();
+    return launch_pdl(gather_kernel, dim3(num_sms * 8), dim3(256), 0, s,
+                      reinterpret_cast<const uint4*>(x), perm, k, H, plan.tiles, plan.mma_tiles,
+                      plan.hdr, reinterpret_cast<uint4*>(x_sorted));
 }
 
 }  // namespace moe

@@ -8,6 +8,20 @@
 namespace moe {
 namespace ptx {
 
+// Programmatic dependent launch.  Every kernel of the library is launched so
+// that it may start while its predecessor on the stream is finishing:
+// grid_dep_wait() blocks until the predecessor grid has completed and its
+// writes are visible, so it comes before the first access to anything an
+// earlier kernel writes or reads; grid_dep_launch() then lets the successor
+// start.  Because every kernel releases its successor only after its own
+// wait, when a kernel starts all kernels before its predecessor are complete.
+__device__ __forceinline__ void grid_dep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // A bounded wait gives up after this many SM cycles (~2 s at 2 GHz).
 constexpr long long kWaitCycles = 4000000000LL;
 

@@ -214,14 +214,15 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
 
 // Producer (one lane): streams the range's items through the weight ring
 // (copy_item) and, if it is the `stager`, stages each unit's activations
-// (copy_act) once the consumers have released the previous unit's.  While a
+// (copy_act) once the consumers have released the previous unit's.  Items
+// [0, pre) (pre <= slots) were already issued into slots [0, pre).  While a
 // slot is still in use the lane sleeps in try_wait.  Returns false on a timeout.
 template <typename ItemFn, typename ActFn>
 __device__ bool produce(const Smem& m, const Range& rg, bool stager, ItemFn copy_item,
-                        ActFn copy_act) {
+                        ActFn copy_act, int pre = 0) {
     if (rg.cnt <= 0) return true;
     int last_round[kMaxSlots];
-    for (int s = 0; s < kMaxSlots; ++s) last_round[s] = -1;
+    for (int s = 0; s < kMaxSlots; ++s) last_round[s] = s < pre ? 0 : -1;
     const int n_units = stager ? rg.u_last - rg.u_first + 1 : 0;
     int act_issued = 0;                       // units whose activations are staged
     if (stager) {
@@ -236,8 +237,8 @@ __device__ bool produce(const Smem& m, const Range& rg, bool stager, ItemFn copy
         }
     };
     bool ok = true;
-    int slot = 0, round = 0;
-    for (int seq = 0; ok && seq < rg.cnt; ++seq) {
+    int slot = pre % m.slots, round = pre / m.slots;
+    for (int seq = pre; ok && seq < rg.cnt; ++seq) {
         if (round > 0) {
             const uint32_t par = (uint32_t)((round - 1) & 1);
             const long long start = clock64();
@@ -605,6 +606,8 @@ thin_gate_up_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
     constexpr int kProducers = 2;   // warp 0 issues the gate rows, warp 1 the up rows
     const int nc = (blockDim.x >> 5) - kProducers;
     const Smem m = smem_setup(smem, stage_bytes, slots, act_bytes, kProducers, nc);
+    grid_dep_wait();      // the plan may come from the previous kernel
+    grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int vec = H / 8;
     const int ipe = I / R;
@@ -659,6 +662,11 @@ thin_down_kernel(const __nv_bfloat16* __restrict__ h, int H, int I, int R,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int vec = I / 8;
     const int ipe = H / R;
+    // The plan was written by the route-list kernels, which precede the
+    // previous kernel on the stream (at least the gate/up kernel runs in
+    // between) and so have completed when this kernel starts; W_down is read
+    // only.  So the CTA's range and its first round of weight rows are
+    // fetched before waiting for the previous kernel; h and y after.
     const Range rg = cta_range(units, hdr, ipe);
     const uint32_t bytes = (uint32_t)R * I * 2;
     const uint32_t hrow = (uint32_t)I * 2;
@@ -666,25 +674,31 @@ thin_down_kernel(const __nv_bfloat16* __restrict__ h, int H, int I, int R,
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t policy = policy_evict_first();
+            auto copy_item = [&](int it, uint32_t dst, uint32_t bar) {
+                const ThinUnit un = units[it / ipe];
+                mbar_expect_tx(bar, bytes);
+                bulk_g2s_evict_first(dst, Wd + ((size_t)un.expert * H + (size_t)(it % ipe) * R) * I,
+                                     bytes, bar, policy);
+            };
+            const int pre = rg.cnt < m.slots ? (rg.cnt > 0 ? rg.cnt : 0) : m.slots;
+            for (int i = 0; i < pre; ++i) copy_item(rg.beg + i, m.buf(i), m.full(i));
+            grid_dep_wait();
+            grid_dep_launch();
             const bool ok = produce(
-                m, rg, true,
-                [&](int it, uint32_t dst, uint32_t bar) {
-                    const ThinUnit un = units[it / ipe];
-                    mbar_expect_tx(bar, bytes);
-                    bulk_g2s_evict_first(
-                        dst, Wd + ((size_t)un.expert * H + (size_t)(it % ipe) * R) * I, bytes,
-                        bar, policy);
-                },
+                m, rg, true, copy_item,
                 [&](int u, uint32_t dst, uint32_t bar) {
                     const ThinUnit un = units[u];
                     // the unit's h rows are consecutive sorted positions
                     mbar_expect_tx(bar, (uint32_t)un.n * hrow);
                     bulk_g2s(dst, h + (size_t)un.row0 * I, (uint32_t)un.n * hrow, bar);
-                });
+                },
+                pre);
             if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
         }
         return;
     }
+    grid_dep_wait();      // consumers write y
+    grid_dep_launch();
 
     constexpr int kExact = (VPL > 0 && DownRegSlots<VPL>::value > 0) ? DownRegSlots<VPL>::value : 16;
     const bool ok = consume<kExact>(m, rg, ipe, units, warp - kProducers, nc, [&]<int N>(int it, int slot) {
@@ -750,9 +764,9 @@ cudaError_t launch_gu(const __nv_bfloat16* x, const int32_t* perm, int k, int H,
     static int done[64];
     cudaError_t e = ensure_smem(thin_gate_up_kernel<V>, done);
     if (e != cudaSuccess) return e;
-    thin_gate_up_kernel<V><<<num_sms, threads_for(g, 2), g.smem, s>>>(
-        x, perm, k, H, I, g.R, Wg, Wu, plan.units, plan.hdr, h, g.stage, g.slots, g.act);
-    return cudaGetLastError();
+    return launch_pdl(thin_gate_up_kernel<V>, dim3(num_sms), dim3(threads_for(g, 2)), g.smem, s,
+                      x, perm, k, H, I, g.R, Wg, Wu, plan.units, plan.hdr, h, g.stage, g.slots,
+                      g.act);
 }
 
 template <int V>
@@ -762,9 +776,8 @@ cudaError_t launch_d(const __nv_bfloat16* h, int H, int I, const __nv_bfloat16* 
     static int done[64];
     cudaError_t e = ensure_smem(thin_down_kernel<V>, done);
     if (e != cudaSuccess) return e;
-    thin_down_kernel<V><<<num_sms, threads_for(g, 1), g.smem, s>>>(
-        h, H, I, g.R, Wd, plan.units, plan.hdr, y, g.stage, g.slots, g.act);
-    return cudaGetLastError();
+    return launch_pdl(thin_down_kernel<V>, dim3(num_sms), dim3(threads_for(g, 1)), g.smem, s, h,
+                      H, I, g.R, Wd, plan.units, plan.hdr, y, g.stage, g.slots, g.act);
 }
 
 }  // namespace

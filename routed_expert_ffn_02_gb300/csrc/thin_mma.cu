@@ -89,8 +89,6 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int total = args.hdr_ro->n_thin_mma * args.n_blocks;
-    if ((int)blockIdx.x >= total) return;   // uniform per CTA: nothing allocated yet
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -115,6 +113,9 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
     __syncthreads();
     fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    grid_dep_wait();      // everything above overlaps the previous kernel
+    grid_dep_launch();
+    const int total = args.hdr_ro->n_thin_mma * args.n_blocks;   // CTAs past it idle
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer ----------------
@@ -280,8 +281,8 @@ cudaError_t launch_thin_mma_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_
     a.w_rows_per_expert = I;
     a.out = h;
     a.ld_out = I;
-    thin_mma_kernel<true><<<num_sms, 256, Cfg<true>::kSmemBytes, s>>>(mX, mG, mU, a);
-    return cudaGetLastError();
+    return launch_pdl(thin_mma_kernel<true>, dim3(num_sms), dim3(256), Cfg<true>::kSmemBytes, s,
+                      mX, mG, mU, a);
 }
 
 cudaError_t launch_thin_mma_down(const __nv_bfloat16* h, int64_t rows_alloc,
@@ -301,8 +302,8 @@ cudaError_t launch_thin_mma_down(const __nv_bfloat16* h, int64_t rows_alloc,
     a.w_rows_per_expert = H;
     a.out = y_sorted;
     a.ld_out = H;
-    thin_mma_kernel<false><<<num_sms, 256, Cfg<false>::kSmemBytes, s>>>(mX, mD, mD, a);
-    return cudaGetLastError();
+    return launch_pdl(thin_mma_kernel<false>, dim3(num_sms), dim3(256), Cfg<false>::kSmemBytes, s,
+                      mX, mD, mD, a);
 }
 
 }  // namespace moe

@@ -143,6 +143,19 @@ def test_forward_threshold_edges(moe, mma_min):
     _full_check(moe, s2, 32, inp, mma_min=mma_min)
 
 
+def test_forward_gemm_pair_boundaries(moe):
+    """The grouped GEMM runs an expert's 128-row tiles in pairs (256 rows per
+    CTA pair): slot counts on either side of pair and tile boundaries, so
+    pairs whose second tile is partial or empty."""
+    counts = [129, 255, 256, 257, 383, 384, 385, 512, 40]
+    E = len(counts)
+    lg = _assigned_logits(counts, E)
+    s = synth.Shape(T=lg.shape[0], E=E, k=1, H=256, I=256)
+    inp = synth.make_layer(s, seed=11)
+    inp["logits"] = lg
+    _full_check(moe, s, 32, inp)
+
+
 def test_forward_one_expert_takes_all(moe):
     s = synth.Shape(T=700, E=4, k=1, H=512, I=256)
     inp = synth.make_layer(s, seed=7)
