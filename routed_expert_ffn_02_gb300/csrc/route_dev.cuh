@@ -1,0 +1,102 @@
+// route_dev.cuh -- the per-token top-k router, shared by the router kernel
+// and the fused small-batch route + route-list kernel.
+//
+// Each token is routed to k of the layer's E experts (dsv41-flash-offload
+// wiki, overview).  Selection compares raw fp32 logits under the total order
+// (value descending, index ascending), so it is exact and needs no
+// arithmetic; gates are a softmax over the k selected logits in fp32.
+//
+// Each lane holds ceil(E/32) candidates as 64-bit keys
+//   key = order(value) << 32 | ~index
+// where order() maps fp32 to an unsigned integer with the same ordering
+// (-0.0 folded onto +0.0, since they compare equal).  The largest key is the
+// next expert to select; k rounds of a warp max-reduction pick the top k in
+// output order.  Key 0 marks an empty or already-taken candidate and sorts
+// below every real logit, including -inf.
+#pragma once
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace routing {
+
+__device__ __forceinline__ uint32_t float_order(float v) {
+    uint32_t u = __float_as_uint(v);
+    if ((u & 0x7fffffffu) == 0u) u = 0u;                 // -0.0 == +0.0
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float order_to_float(uint32_t o) {
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
+// One warp routes one token: writes idx[0, k) (experts in selection order)
+// and gates[0, k).  All 32 lanes call it together.
+template <int EPL>   // candidates per lane
+__device__ __forceinline__ void route_row(const float* __restrict__ row, int E, int k,
+                                          int32_t* __restrict__ idx, float* __restrict__ gates) {
+    const int lane = threadIdx.x & 31;
+    uint64_t key[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+        const int e = lane + 32 * j;
+        key[j] = (e < E) ? ((uint64_t)float_order(__ldg(row + e)) << 32) |
+                               (uint64_t)(~(uint32_t)e)
+                         : 0ull;
+    }
+
+    float sel_val[kMaxK];
+    int sel_idx[kMaxK];
+#pragma unroll
+    for (int r = 0; r < kMaxK; ++r) {
+        sel_val[r] = 0.f;
+        sel_idx[r] = 0;
+        if (r < k) {
+            uint64_t best = 0ull;
+#pragma unroll
+            for (int j = 0; j < EPL; ++j) best = key[j] > best ? key[j] : best;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
+                best = o > best ? o : best;
+            }
+            // The owner retires the winner (keys are unique: indices differ).
+#pragma unroll
+            for (int j = 0; j < EPL; ++j)
+                if (key[j] == best) key[j] = 0ull;
+            sel_val[r] = order_to_float((uint32_t)(best >> 32));
+            sel_idx[r] = (int)(~(uint32_t)(best & 0xffffffffull));
+        }
+    }
+
+    // Softmax over the selection, relative to the largest selected logit.
+    const float m = sel_val[0];
+    float w[kMaxK];
+    float denom = 0.f;
+#pragma unroll
+    for (int r = 0; r < kMaxK; ++r) {
+        w[r] = (r < k) ? expf(sel_val[r] - m) : 0.f;
+        denom += w[r];
+    }
+    // Lane r writes output r (coalesced).
+#pragma unroll
+    for (int r = 0; r < kMaxK; ++r) {
+        if (r < k && lane == r) {
+            idx[r] = sel_idx[r];
+            gates[r] = w[r] / denom;
+        }
+    }
+}
+
+// Candidates per lane for E experts: the smallest of 1, 2, 4, 8, 12, 16, 24,
+// 32 that covers E (E <= 1024).
+inline int candidates_per_lane(int E) {
+    const int epl = (E + 31) / 32;
+    const int steps[] = {1, 2, 4, 8, 12, 16, 24, 32};
+    for (int v : steps)
+        if (epl <= v) return v;
+    return 32;
+}
+
+}  // namespace routing
+}  // namespace moe
