@@ -74,32 +74,43 @@ def load_peaks():
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons while running."""
+    """Samples nvidia-smi clocks and throttle reasons every 100 ms while
+    running; each sample carries its host time so a timed window can be
+    picked out (mark() brackets it)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.samples = []          # (host time, line)
+        self.window = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t_end = time.monotonic() + 5.0          # sampling is live before timing
+            while not self.samples and time.monotonic() < t_end:
+                time.sleep(0.01)
         except OSError:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.samples.append((time.monotonic(), line.strip()))
+
+    def mark(self, t0: float, t1: float):
+        """The timed window, in time.monotonic() seconds."""
+        self.window = (t0, t1)
 
     def __exit__(self, *exc):
         if self.proc:
@@ -109,10 +120,9 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def _parse(self, lines):
         sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 7:
                 continue
@@ -121,13 +131,28 @@ class ClockSampler:
                 mx.append(float(parts[1]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[3:7]):
+            for n, v in zip(self.NAMES, parts[3:7]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
-        if not sm:
+        return sm, mx, reasons
+
+    def summary(self):
+        lines = [l for _, l in self.samples]
+        if self.window:
+            t0, t1 = self.window
+            inside = [l for t, l in self.samples if t0 <= t <= t1]
+        else:
+            inside = lines
+        sm, mx, reasons = self._parse(inside)
+        all_sm, all_mx, all_reasons = self._parse(lines)
+        if not all_sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else max(all_mx),
+               "reasons": sorted(reasons), "samples": len(sm),
+               "run": {"sm_mhz_median": statistics.median(all_sm), "sm_mhz_min": min(all_sm),
+                       "reasons": sorted(all_reasons), "samples": len(all_sm)}}
+        return out
 
 
 # --------------------------------------------------------------- workload
@@ -218,7 +243,7 @@ class Layer:
         return c.cpu().numpy()
 
 
-def time_steps(layer, steps, warmup, profiled=True, rotate=True):
+def time_steps(layer, steps, warmup, profiled=True, rotate=True, clk=None):
     moe = layer.moe
     for i in range(warmup):
         layer.forward(i)
@@ -228,12 +253,16 @@ def time_steps(layer, steps, warmup, profiled=True, rotate=True):
     end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     barrier()
+    t0 = time.monotonic()
     start.record()
     for i in range(steps):
         layer.forward(i if rotate else 0, events=ev[i] if profiled else None)
     end.record()
     torch.cuda.synchronize()
+    t1 = time.monotonic()
     barrier()
+    if clk is not None:
+        clk.mark(t0, t1)
     total_ms = start.elapsed_time(end)
     stage_ms = None
     if profiled:
@@ -510,7 +539,7 @@ def run_gpu(args):
     work = stage_work(shape, counts)
 
     with ClockSampler(local) as clk:
-        total_ms, stage_ms = time_steps(layer, args.steps, args.warmup)
+        total_ms, stage_ms = time_steps(layer, args.steps, args.warmup, clk=clk)
     total_ms = max_over_ranks(total_ms)
     ms_per_step = total_ms / args.steps
     value = world * shape.T * args.steps / (total_ms * 1e-3)
