@@ -502,6 +502,9 @@ def run_offload(args, moe, dev, n_layers=12, n_slots=8):
     torch.cuda.synchronize()
     layer_ms = c0.elapsed_time(c1) / 5
     st.close()
+    del st
+    torch.cuda.empty_cache()
+    cached = run_offload_decode_cache(moe, dev, host, s, n_layers)
     # the stager copies only the experts each layer's tokens are routed to
     touched = []
     for l in range(n_layers):
@@ -519,6 +522,70 @@ def run_offload(args, moe, dev, n_layers=12, n_slots=8):
         "h2d_gbs": round(copied / (ms * 1e-3) / 1e9, 1),
         "compute_ms_per_layer_resident": round(layer_ms, 3),
         "bound": "host-to-device copy" if ms > n_layers * layer_ms * 1.2 else "compute",
+        "decode_with_expert_cache": cached,
+    }
+
+
+def run_offload_decode_cache(moe, dev, host, s, n_layers, B=4, n_slots=1536, warm=16, steps=16):
+    """Decode batch B through the same offloaded layers (experts in pinned
+    host memory): one step is B tokens through all layers.  With an HBM
+    expert cache of n_slots experts (least recently used evicted) against the
+    stager, which copies every touched expert of every layer at every step.
+    Each step draws new logits (same Zipf(1.1) expert popularity per layer)."""
+    shape = moe.Shape(B, s.E, s.k, s.H, s.I, FAT_THRESHOLD)
+    x = synth.make_x(B, s.H, seed=0).to(dev)
+    n_sets = warm + steps
+    lg = [[synth.make_logits(B, s.E, seed=0, layer=l, rep=r, zipf_s=synth.ZIPF_S).to(dev)
+           for l in range(n_layers)] for r in range(n_sets)]
+    outs = [torch.empty((B, s.H), dtype=torch.bfloat16, device=dev) for _ in range(n_layers)]
+    ws = moe.Workspace(moe.workspace_size(shape), dev)
+    compute = torch.cuda.current_stream()
+    copy = torch.cuda.Stream(device=dev)
+    ids = list(range(n_layers))
+
+    cache = moe.ExpertCache(shape, n_slots, n_layers, dev)
+    for r in range(warm):
+        cache.forward(ids, lg[r], x, host, outs, ws, compute, copy)
+    torch.cuda.synchronize()
+    h0, m0 = cache.stats()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for r in range(warm, n_sets):
+        cache.forward(ids, lg[r], x, host, outs, ws, compute, copy)
+    t1.record()
+    torch.cuda.synchronize()
+    ms_cache = t0.elapsed_time(t1) / steps
+    h1, m1 = cache.stats()
+    cache.close()
+    del cache
+    torch.cuda.empty_cache()
+
+    st = moe.Stager(shape, 8, dev)
+    for r in range(2):
+        st.forward(shape, lg[r], x, host, outs, ws, compute, copy)
+    torch.cuda.synchronize()
+    n_st = 4
+    t0.record()
+    for r in range(warm, warm + n_st):
+        st.forward(shape, lg[r], x, host, outs, ws, compute, copy)
+    t1.record()
+    torch.cuda.synchronize()
+    ms_stream = t0.elapsed_time(t1) / n_st
+    st.close()
+    del st
+    torch.cuda.empty_cache()
+    hits, misses = h1 - h0, m1 - m0
+    return {
+        "workload": f"decode batch {B} through {n_layers} offloaded layers (384 experts, H=2048, "
+                    f"I=1024), HBM cache of {n_slots} experts "
+                    f"({n_slots * moe.layer_weight_bytes(shape) // s.E / 1e9:.1f} GB)",
+        "ms_per_step_cached": round(ms_cache, 3),
+        "tokens_per_s_cached": round(B / (ms_cache * 1e-3), 1),
+        "hit_rate": round(hits / max(hits + misses, 1), 4),
+        "misses_per_step": round(misses / steps, 1),
+        "ms_per_step_streamed": round(ms_stream, 3),
+        "tokens_per_s_streamed": round(B / (ms_stream * 1e-3), 1),
     }
 
 

@@ -265,6 +265,50 @@ moe_status moe_forward_offload(moe_stager* stager, const moe_shape* shape, int32
                                void* ws, size_t ws_bytes, moe_stream_t compute,
                                moe_stream_t copy);
 
+/* ---- expert cache (models larger than HBM) ---------------------------- */
+
+/* An HBM-resident expert cache in front of experts kept in host memory
+ * (dsv41-flash-offload wiki, overview and file map: a VRAM expert cache over
+ * experts in host RAM).  n_slots expert slots live in one caller-owned device
+ * block; an expert of any layer stays resident across calls until it is the
+ * least recently used one and its slot is needed. */
+typedef struct moe_cache moe_cache;
+
+/* Bytes of the device block for n_slots slots (each one expert's W_gate, W_up
+ * and W_down) and per-layer expert -> slot tables for up to max_layers layers
+ * per call (0 for invalid arguments). */
+size_t moe_cache_bytes(const moe_shape* shape, int32_t n_slots, int32_t max_layers);
+
+/* Creates a cache for experts of shape->E, H, I over `mem` (device,
+ * moe_cache_bytes bytes, 256-byte aligned, caller-owned, outliving the cache
+ * and every forward enqueued with it).  The cache owns 2 x max_layers CUDA
+ * events and pinned host staging (max_layers x E x 5 bytes). */
+moe_status moe_cache_create(const moe_shape* shape, int32_t n_slots, int32_t max_layers,
+                            void* mem, size_t mem_bytes, moe_cache** out);
+moe_status moe_cache_destroy(moe_cache* cache);
+
+/* Expert lookups since creation that found the expert resident / copied it. */
+moe_status moe_cache_stats(const moe_cache* cache, int64_t* hits, int64_t* misses);
+
+/* Runs n_layers independent layers on x [T, H] (device) with logits[l]
+ * [T, E] and out[l] [T, H] (device); layer l's experts are host_weights[l]
+ * (pinned host memory, W_gate | W_up | W_down as for moe_forward_offload),
+ * cached under the key (layer_ids[l], expert), layer_ids[l] >= 0.  First every
+ * layer is routed on `compute` and its touched experts marked in pinned host
+ * flags; the call synchronises `compute` once to read them.  Then, per layer:
+ * each touched expert not resident is copied on `copy` into the least
+ * recently used slot that layer l does not need, once the compute of the
+ * last layer that read the slot has finished; the layer runs on `compute`
+ * once its copies have landed.  n_layers <= max_layers; every layer must
+ * touch at most n_slots experts (else MOE_ERR_INVALID_ARG, with the earlier
+ * layers already enqueued).  `copy` must differ from `compute`; ws as for
+ * moe_forward.  Errors as moe_forward. */
+moe_status moe_forward_cached(moe_cache* cache, const moe_shape* shape, int32_t n_layers,
+                              const int32_t* layer_ids, const float* const* logits,
+                              const moe_bf16* x, const void* const* host_weights,
+                              moe_bf16* const* out, void* ws, size_t ws_bytes,
+                              moe_stream_t compute, moe_stream_t copy);
+
 /* ---- activations in host memory --------------------------------------- */
 
 /* The layer on host-resident activations, as a serving process feeds it:

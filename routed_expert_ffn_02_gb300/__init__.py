@@ -10,5 +10,5 @@ from .binding import (  # noqa: F401
     moe_combine, moe_forward, moe_forward_profiled, workspace_size, permute_workspace_size,
     expert_ffn_workspace_size, version, LIB_PATH, EXPORTED,
     PROFILE_EVENTS, PROFILE_STAGES, forward_launches, Stager, layer_weight_bytes,
-    pack_layer_weights, Pipe, pipe_workspace_size, DecodeGraph,
+    pack_layer_weights, Pipe, pipe_workspace_size, DecodeGraph, ExpertCache,
 )

@@ -38,7 +38,8 @@ EXPORTED = ("moe_route", "moe_permute_workspace_size", "moe_permute", "moe_permu
             "moe_stager_destroy", "moe_forward_offload", "moe_workspace_init",
             "moe_workspace_status", "moe_last_error", "moe_version",
             "moe_pipe_workspace_size", "moe_pipe_create", "moe_pipe_destroy",
-            "moe_forward_host")
+            "moe_forward_host", "moe_cache_bytes", "moe_cache_create", "moe_cache_destroy",
+            "moe_cache_stats", "moe_forward_cached")
 
 
 class MoeShape(ctypes.Structure):
@@ -99,6 +100,12 @@ _sig = {
                              ctypes.POINTER(_P), _P, _sz, _P, _P], _i32),
     "moe_workspace_init": ([_P, _sz, _P], _i32),
     "moe_pipe_workspace_size": ([_SP], _sz),
+    "moe_cache_bytes": ([_SP, _i32, _i32], _sz),
+    "moe_cache_create": ([_SP, _i32, _i32, _P, _sz, ctypes.POINTER(_P)], _i32),
+    "moe_cache_destroy": ([_P], _i32),
+    "moe_cache_stats": ([_P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)], _i32),
+    "moe_forward_cached": ([_P, _SP, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_P), _P,
+                            ctypes.POINTER(_P), ctypes.POINTER(_P), _P, _sz, _P, _P], _i32),
     "moe_pipe_create": ([ctypes.POINTER(_P)], _i32),
     "moe_pipe_destroy": ([_P], _i32),
     "moe_forward_host": ([_P, _SP, _P, _P, _P, _P, _P, _P, _P, _sz, _P, _P, _P], _i32),
@@ -393,6 +400,66 @@ class Pipe:
 
     def synchronize(self):
         self.d2h.synchronize()
+
+
+class ExpertCache:
+    """HBM expert cache (n_slots experts, least recently used evicted) over
+    experts kept in pinned host memory; owns its device block (torch) and the
+    library's cache."""
+
+    def __init__(self, shape: Shape, n_slots: int, max_layers: int, device=None):
+        device = device or torch.device("cuda", torch.cuda.current_device())
+        self.shape = shape
+        nbytes = _lib.moe_cache_bytes(ctypes.byref(shape.c()), n_slots, max_layers)
+        if nbytes == 0:
+            raise MoeError(1, "moe_cache_bytes")
+        self._mem = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+        off = (-self._mem.data_ptr()) % 256
+        self.mem = self._mem[off:off + nbytes]
+        self._h = ctypes.c_void_p()
+        _check(_lib.moe_cache_create(ctypes.byref(shape.c()), n_slots, max_layers,
+                                     ctypes.c_void_p(self.mem.data_ptr()), nbytes,
+                                     ctypes.byref(self._h)), "moe_cache_create")
+
+    def close(self):
+        if self._h:
+            _lib.moe_cache_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def stats(self):
+        """(hits, misses) since creation."""
+        h, m = ctypes.c_int64(), ctypes.c_int64()
+        _check(_lib.moe_cache_stats(self._h, ctypes.byref(h), ctypes.byref(m)), "moe_cache_stats")
+        return h.value, m.value
+
+    def forward(self, layer_ids, logits, x, host_weights, outs=None, ws: Workspace | None = None,
+                compute=None, copy=None):
+        """Runs len(layer_ids) layers: logits[l], outs[l] device tensors,
+        host_weights[l] pinned blocks from pack_layer_weights."""
+        L = len(layer_ids)
+        dev = x.device
+        shape = self.shape
+        outs = outs if outs is not None else [
+            torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+        ws = ws or Workspace(workspace_size(shape), dev, compute)
+        compute = compute if compute is not None else torch.cuda.current_stream()
+        copy = copy if copy is not None else torch.cuda.Stream(device=dev)
+        PA = ctypes.c_void_p * max(L, 1)
+        ids = (ctypes.c_int32 * max(L, 1))(*layer_ids)
+        lg = PA(*[ctypes.c_void_p(t.data_ptr()) for t in logits])
+        hw = PA(*[ctypes.c_void_p(t.data_ptr()) for t in host_weights])
+        op = PA(*[ctypes.c_void_p(t.data_ptr()) for t in outs])
+        _check(_lib.moe_forward_cached(self._h, ctypes.byref(shape.c()), L, ids, lg, _ptr(x), hw,
+                                       op, ws.ptr, ws.nbytes,
+                                       ctypes.c_void_p(compute.cuda_stream),
+                                       ctypes.c_void_p(copy.cuda_stream)), "moe_forward_cached")
+        return outs
 
 
 class DecodeGraph:

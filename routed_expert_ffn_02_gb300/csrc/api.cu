@@ -144,7 +144,7 @@ ExpertKernels expert_kernels(const moe_shape* sh, int64_t fat_bound) {
 Plan make_plan(const moe_shape* sh, FatTile* tiles, ThinUnit* units, FatTile* mma_tiles,
                WsHeader* hdr) {
     return Plan{tiles, units, mma_tiles, hdr, sh->fat_threshold,
-                thin_unit_tokens(sh->H, sh->I), thin_mma_min(sh)};
+                thin_unit_tokens(sh->H, sh->I), thin_mma_min(sh), nullptr, sh->E};
 }
 
 // Bump allocator over the caller's workspace (256-byte aligned regions).
@@ -408,7 +408,8 @@ static moe_status forward_impl(const moe_shape* shape, const float* logits, cons
                                const moe_bf16* W_gate, const moe_bf16* W_up,
                                const moe_bf16* W_down, moe_bf16* out, int32_t* topk_idx,
                                float* gates, void* ws, size_t ws_bytes, moe_stream_t stream,
-                               cudaEvent_t* ev) {
+                               cudaEvent_t* ev, const int32_t* wslot = nullptr,
+                               int32_t n_wblocks = 0) {
     moe_status st = check_shape(shape);
     if (st != MOE_OK) return st;
     if (shape->T == 0) return ok();
@@ -427,7 +428,11 @@ static moe_status forward_impl(const moe_shape* shape, const float* logits, cons
     CUDA_TRY(mark(ev, kEvStart, s), "cudaEventRecord");
     CUDA_TRY(launch_route(logits, T, E, k, idx, g, s), "route");
     CUDA_TRY(mark(ev, kEvRoute, s), "cudaEventRecord");
-    const Plan plan = make_plan(shape, b.tiles, b.units, b.mma_tiles, b.hdr);
+    Plan plan = make_plan(shape, b.tiles, b.units, b.mma_tiles, b.hdr);
+    if (wslot) {
+        plan.wslot = wslot;
+        plan.n_wblocks = n_wblocks;
+    }
     const int64_t P = (int64_t)T * k;
     const int64_t nch = (P + kPermChunk - 1) / kPermChunk;
     CUDA_TRY(launch_permute(idx, T, E, k, b.counts, b.offsets, b.perm, b.inv_perm, b.chunk,
@@ -444,6 +449,15 @@ static moe_status forward_impl(const moe_shape* shape, const float* logits, cons
                             dev.num_sms, s), "combine");
     CUDA_TRY(mark(ev, kEvCombine, s), "cudaEventRecord");
     return ok();
+}
+
+moe_status moe::forward_blocks(const moe_shape* shape, const float* logits, const moe_bf16* x,
+                              const moe_bf16* W_gate, const moe_bf16* W_up,
+                              const moe_bf16* W_down, const int32_t* wslot, int32_t n_wblocks,
+                              moe_bf16* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    if (!wslot || n_wblocks < 1) return fail(MOE_ERR_INVALID_ARG, "bad weight-block table");
+    return forward_impl(shape, logits, x, W_gate, W_up, W_down, out, nullptr, nullptr, ws,
+                        ws_bytes, stream, nullptr, wslot, n_wblocks);
 }
 
 extern "C" {

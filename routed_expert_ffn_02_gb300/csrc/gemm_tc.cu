@@ -68,6 +68,7 @@ constexpr uint16_t kPairMask = 0x3;
 
 struct GemmArgs {
     const FatTile* tiles;  // pairs: tiles 2q, 2q+1 belong to one expert
+    const int32_t* wslot;  // expert -> weight block (nullptr: identity)
     const WsHeader* hdr_ro;
     WsHeader* hdr;
     int n_blocks_n;        // N tiles per expert
@@ -147,7 +148,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             const int pair = w / args.n_blocks_n;
             const int nt = w % args.n_blocks_n;
             const FatTile ft = args.tiles[2 * pair + (int)rank];
-            const int brow = ft.expert * args.b_rows_per_expert + nt * (kGated ? BM : BN_MMA) +
+            const int brow = weight_block(args.wslot, ft.expert) * args.b_rows_per_expert +
+                             nt * (kGated ? BM : BN_MMA) +
                              (int)rank * args.b_half_rows;
             for (int kb = 0; kb < args.k_blocks; ++kb) {
                 if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
@@ -388,13 +390,14 @@ cudaError_t launch_gemm_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_allo
     CUtensorMap mA, mG, mU;
     cudaError_t e;
     if ((e = make_tma_map_bf16(&mA, x_sorted, (uint64_t)rows_alloc, (uint64_t)H, BM)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16(&mG, Wg, (uint64_t)E * I, (uint64_t)H, 128)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16(&mU, Wu, (uint64_t)E * I, (uint64_t)H, 128)) != cudaSuccess) return e;
+    if ((e = make_tma_map_bf16(&mG, Wg, (uint64_t)plan.n_wblocks * I, (uint64_t)H, 128)) != cudaSuccess) return e;
+    if ((e = make_tma_map_bf16(&mU, Wu, (uint64_t)plan.n_wblocks * I, (uint64_t)H, 128)) != cudaSuccess) return e;
     if ((e = set_smem_attr<true>()) != cudaSuccess) return e;
     int grid = 0;
     if ((e = pair_grid<true>(num_sms, &grid)) != cudaSuccess) return e;
     GemmArgs a;
     a.tiles = plan.tiles;
+    a.wslot = plan.wslot;
     a.hdr_ro = plan.hdr;
     a.hdr = plan.hdr;
     a.n_blocks_n = I / 128;
@@ -415,12 +418,13 @@ cudaError_t launch_gemm_down(const __nv_bfloat16* h, int64_t rows_alloc,
     CUtensorMap mA, mD;
     cudaError_t e;
     if ((e = make_tma_map_bf16(&mA, h, (uint64_t)rows_alloc, (uint64_t)I, BM)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16(&mD, Wd, (uint64_t)E * H, (uint64_t)I, 128)) != cudaSuccess) return e;
+    if ((e = make_tma_map_bf16(&mD, Wd, (uint64_t)plan.n_wblocks * H, (uint64_t)I, 128)) != cudaSuccess) return e;
     if ((e = set_smem_attr<false>()) != cudaSuccess) return e;
     int grid = 0;
     if ((e = pair_grid<false>(num_sms, &grid)) != cudaSuccess) return e;
     GemmArgs a;
     a.tiles = plan.tiles;
+    a.wslot = plan.wslot;
     a.hdr_ro = plan.hdr;
     a.hdr = plan.hdr;
     a.n_blocks_n = H / 256;

@@ -99,7 +99,16 @@ struct Plan {
     int32_t fat_threshold;
     int32_t unit_tokens; // slots per weight-streaming unit (thin_unit_tokens)
     int32_t thin_mma_min;
+    // Weight blocks: expert e's matrices are block wslot[e] of W_gate / W_up /
+    // W_down, which hold n_wblocks blocks (wslot == nullptr: block e, E blocks).
+    const int32_t* wslot;
+    int32_t n_wblocks;
 };
+
+// Weight block of expert e (see Plan::wslot).
+__device__ __forceinline__ int weight_block(const int32_t* wslot, int e) {
+    return wslot ? __ldg(wslot + e) : e;
+}
 
 // By default every thin expert streams on the tensor cores once at least this
 // many 128-row gate/up work items can exist (touched experts x I/128), and
@@ -181,6 +190,13 @@ cudaError_t launch_combine(const __nv_bfloat16* y_sorted, const int32_t* inv_per
 // sets flags[e] = 1 for each expert the layer touches (asynchronous on s).
 moe_status mark_touched_experts(const moe_shape* shape, const float* logits, void* ws,
                                 size_t ws_bytes, uint8_t* flags, cudaStream_t s);
+
+// moe_forward with expert e's weights in block wslot[e] (device table of E
+// entries) of W_gate / W_up / W_down, which hold n_wblocks blocks.
+moe_status forward_blocks(const moe_shape* shape, const float* logits, const moe_bf16* x,
+                          const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
+                          const int32_t* wslot, int32_t n_wblocks, moe_bf16* out, void* ws,
+                          size_t ws_bytes, moe_stream_t stream);
 
 // Validates a moe_shape as every entry point does (sets moe_last_error()).
 moe_status check_shape_status(const moe_shape* shape);

@@ -600,6 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 thin_gate_up_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ perm,
                     int k, int H, int I, int R, const __nv_bfloat16* __restrict__ Wg,
                     const __nv_bfloat16* __restrict__ Wu, const ThinUnit* __restrict__ units,
+                    const int32_t* __restrict__ wslot,
                     WsHeader* hdr, __nv_bfloat16* __restrict__ h, int stage_bytes, int slots,
                     int act_bytes) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -624,7 +625,8 @@ thin_gate_up_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
                 m, rg, warp == 0,
                 [&](int it, uint32_t dst, uint32_t bar) {
                     const ThinUnit un = units[it / ipe];
-                    const size_t off = ((size_t)un.expert * I + (size_t)(it % ipe) * R) * H;
+                    const size_t off =
+                        ((size_t)weight_block(wslot, un.expert) * I + (size_t)(it % ipe) * R) * H;
                     mbar_expect_tx(bar, half);
                     bulk_g2s_evict_first(dst + part, W + off, half, bar, policy);
                 },
@@ -653,8 +655,8 @@ template <int VPL>
 __global__ void __launch_bounds__(kThreads, 1)
 thin_down_kernel(const __nv_bfloat16* __restrict__ h, int H, int I, int R,
                  const __nv_bfloat16* __restrict__ Wd, const ThinUnit* __restrict__ units,
-                 WsHeader* hdr, __nv_bfloat16* __restrict__ y, int stage_bytes, int slots,
-                 int act_bytes) {
+                 const int32_t* __restrict__ wslot, WsHeader* hdr,
+                 __nv_bfloat16* __restrict__ y, int stage_bytes, int slots, int act_bytes) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kProducers = 1;
     const int nc = (blockDim.x >> 5) - kProducers;
@@ -677,8 +679,9 @@ thin_down_kernel(const __nv_bfloat16* __restrict__ h, int H, int I, int R,
             auto copy_item = [&](int it, uint32_t dst, uint32_t bar) {
                 const ThinUnit un = units[it / ipe];
                 mbar_expect_tx(bar, bytes);
-                bulk_g2s_evict_first(dst, Wd + ((size_t)un.expert * H + (size_t)(it % ipe) * R) * I,
-                                     bytes, bar, policy);
+                bulk_g2s_evict_first(
+                    dst, Wd + ((size_t)weight_block(wslot, un.expert) * H + (size_t)(it % ipe) * R) * I,
+                    bytes, bar, policy);
             };
             const int pre = rg.cnt < m.slots ? (rg.cnt > 0 ? rg.cnt : 0) : m.slots;
             for (int i = 0; i < pre; ++i) copy_item(rg.beg + i, m.buf(i), m.full(i));
@@ -765,8 +768,8 @@ cudaError_t launch_gu(const __nv_bfloat16* x, const int32_t* perm, int k, int H,
     cudaError_t e = ensure_smem(thin_gate_up_kernel<V>, done);
     if (e != cudaSuccess) return e;
     return launch_pdl(thin_gate_up_kernel<V>, dim3(num_sms), dim3(threads_for(g, 2)), g.smem, s,
-                      x, perm, k, H, I, g.R, Wg, Wu, plan.units, plan.hdr, h, g.stage, g.slots,
-                      g.act);
+                      x, perm, k, H, I, g.R, Wg, Wu, plan.units, plan.wslot, plan.hdr, h, g.stage,
+                      g.slots, g.act);
 }
 
 template <int V>
@@ -777,7 +780,7 @@ cudaError_t launch_d(const __nv_bfloat16* h, int H, int I, const __nv_bfloat16* 
     cudaError_t e = ensure_smem(thin_down_kernel<V>, done);
     if (e != cudaSuccess) return e;
     return launch_pdl(thin_down_kernel<V>, dim3(num_sms), dim3(threads_for(g, 1)), g.smem, s, h,
-                      H, I, g.R, Wd, plan.units, plan.hdr, y, g.stage, g.slots, g.act);
+                      H, I, g.R, Wd, plan.units, plan.wslot, plan.hdr, y, g.stage, g.slots, g.act);
 }
 
 }  // namespace

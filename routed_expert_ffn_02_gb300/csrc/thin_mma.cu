@@ -58,6 +58,7 @@ struct Cfg {
 
 struct ThinMmaArgs {
     const FatTile* tiles;     // thin experts on this kernel: (expert, row0, n)
+    const int32_t* wslot;     // expert -> weight block (nullptr: identity)
     const WsHeader* hdr_ro;
     WsHeader* hdr;
     int n_blocks;             // 128-row weight blocks per expert
@@ -126,7 +127,8 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
             const FatTile ft = args.tiles[t / args.n_blocks];
-            const int wrow = ft.expert * args.w_rows_per_expert + (t % args.n_blocks) * BM;
+            const int wrow = weight_block(args.wslot, ft.expert) * args.w_rows_per_expert +
+                             (t % args.n_blocks) * BM;
             for (int kb = 0; kb < args.k_blocks; ++kb) {
                 if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
                     ok = false;
@@ -269,11 +271,12 @@ cudaError_t launch_thin_mma_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_
     CUtensorMap mX, mG, mU;
     cudaError_t e;
     if ((e = make_tma_map_bf16(&mX, x_sorted, (uint64_t)rows_alloc, (uint64_t)H, BN)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16(&mG, Wg, (uint64_t)E * I, (uint64_t)H, BM)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16(&mU, Wu, (uint64_t)E * I, (uint64_t)H, BM)) != cudaSuccess) return e;
+    if ((e = make_tma_map_bf16(&mG, Wg, (uint64_t)plan.n_wblocks * I, (uint64_t)H, BM)) != cudaSuccess) return e;
+    if ((e = make_tma_map_bf16(&mU, Wu, (uint64_t)plan.n_wblocks * I, (uint64_t)H, BM)) != cudaSuccess) return e;
     if ((e = set_smem_attr<true>()) != cudaSuccess) return e;
     ThinMmaArgs a;
     a.tiles = plan.mma_tiles;
+    a.wslot = plan.wslot;
     a.hdr_ro = plan.hdr;
     a.hdr = plan.hdr;
     a.n_blocks = I / BM;
@@ -291,10 +294,11 @@ cudaError_t launch_thin_mma_down(const __nv_bfloat16* h, int64_t rows_alloc,
     CUtensorMap mX, mD;
     cudaError_t e;
     if ((e = make_tma_map_bf16(&mX, h, (uint64_t)rows_alloc, (uint64_t)I, BN)) != cudaSuccess) return e;
-    if ((e = make_tma_map_bf16(&mD, Wd, (uint64_t)E * H, (uint64_t)I, BM)) != cudaSuccess) return e;
+    if ((e = make_tma_map_bf16(&mD, Wd, (uint64_t)plan.n_wblocks * H, (uint64_t)I, BM)) != cudaSuccess) return e;
     if ((e = set_smem_attr<false>()) != cudaSuccess) return e;
     ThinMmaArgs a;
     a.tiles = plan.mma_tiles;
+    a.wslot = plan.wslot;
     a.hdr_ro = plan.hdr;
     a.hdr = plan.hdr;
     a.n_blocks = H / BM;

@@ -169,3 +169,22 @@ def test_pipe_argument_errors(moe):
     assert b"different streams" in lib.moe_last_error()
     assert lib.moe_forward_host(fake, ctypes.byref(bad), *args, s1, s2, s3) == 1
     assert lib.moe_pipe_create(None) == 1
+
+
+def test_cache_argument_errors(moe):
+    """moe_cache_bytes sizing and argument checks made before any CUDA call."""
+    lib = moe.binding.raw_lib()
+    shape = moe.binding.MoeShape(16, 32, 4, 512, 256, 32)
+    per_expert = 512 * 256 * 2
+    tables = (3 * 32 * 4 + 255) // 256 * 256
+    assert lib.moe_cache_bytes(ctypes.byref(shape), 10, 3) == 3 * 10 * per_expert + tables
+    assert lib.moe_cache_bytes(ctypes.byref(shape), 0, 3) == 0
+    assert lib.moe_cache_bytes(ctypes.byref(shape), 10, 0) == 0
+    out = ctypes.c_void_p()
+    assert lib.moe_cache_create(ctypes.byref(shape), 10, 3, None, 0, ctypes.byref(out)) == 1
+    assert lib.moe_cache_create(ctypes.byref(shape), 10, 3, ctypes.c_void_p(256), 16,
+                                ctypes.byref(out)) == 1     # below moe_cache_bytes
+    assert lib.moe_forward_cached(None, ctypes.byref(shape), 0, None, None, None, None, None,
+                                  None, 0, None, None) == 1
+    h, m = ctypes.c_int64(), ctypes.c_int64()
+    assert lib.moe_cache_stats(None, ctypes.byref(h), ctypes.byref(m)) == 1
