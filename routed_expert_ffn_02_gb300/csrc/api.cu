@@ -44,8 +44,6 @@ moe_status cuda_fail(cudaError_t e, const char* where) {
     return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
 }
 
-constexpr int kMaxDevices = 64;
-
 struct DeviceInfo {
     int checked = 0;
     int supported = 0;

@@ -331,20 +331,15 @@ EncodeTiledFn encode_fn() {
 
 template <bool kGated>
 cudaError_t set_smem_attr() {
-    static cudaError_t err = cudaErrorUnknown;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute(grouped_gemm_kernel<kGated>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    });
-    return err;
+    static std::atomic<int> done[kMaxDevices];
+    return smem_limit_once(grouped_gemm_kernel<kGated>, SMEM_BYTES, done);
 }
 
 // CTAs to launch: two per co-resident cluster (an SM pair whose partner is
 // busy or absent cannot host a cluster, so this can be below the SM count).
 template <bool kGated>
 cudaError_t pair_grid(int num_sms, int* grid) {
-    constexpr int kMaxDev = 64;
+    constexpr int kMaxDev = kMaxDevices;
     static int cached[kMaxDev] = {};
     static std::mutex mu;
     int dev = 0;

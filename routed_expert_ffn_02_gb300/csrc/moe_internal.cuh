@@ -8,6 +8,8 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <atomic>
+
 #include "moe.h"
 
 namespace moe {
@@ -55,6 +57,22 @@ struct ThinUnit {
 __host__ __device__ inline int thin_unit_cost(int n) { return (n < 4 ? 4 : n) + 2; }
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+constexpr int kMaxDevices = 64;
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device (`done`: one flag per device, per kernel).
+template <typename K>
+cudaError_t smem_limit_once(K kernel, int bytes, std::atomic<int> (&done)[kMaxDevices]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done[dev].store(1, std::memory_order_release);
+    return e;
+}
 
 // Programmatic dependent launch is on for the calling thread's launches while
 // a PdlScope(true) is alive.  The layer entry points turn it on for small

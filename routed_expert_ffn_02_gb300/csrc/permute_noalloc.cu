@@ -37,7 +37,6 @@ constexpr size_t kScratchBytes = sizeof(WsHeader) + kScratchInts * sizeof(int32_
 // [WsHeader | chunk_hist | chunk_base]
 static __device__ __align__(256) unsigned char g_permute_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 

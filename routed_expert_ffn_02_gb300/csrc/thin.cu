@@ -745,27 +745,12 @@ int threads_for(const Geometry& g, int producers) {
     return 32 * (producers + consumers);
 }
 
-// Raises a kernel's dynamic shared-memory limit once per device (the launch
-// path then makes no extra runtime calls).
-template <typename K>
-cudaError_t ensure_smem(K kernel, int (&done)[64]) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBudget + 1024);
-    if (e == cudaSuccess) done[dev] = 1;
-    return e;
-}
-
 template <int V>
 cudaError_t launch_gu(const __nv_bfloat16* x, const int32_t* perm, int k, int H, int I,
                       const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, const Plan& plan,
                       const Geometry& g, __nv_bfloat16* h, int num_sms, cudaStream_t s) {
-    static int done[64];
-    cudaError_t e = ensure_smem(thin_gate_up_kernel<V>, done);
+    static std::atomic<int> done[kMaxDevices];
+    cudaError_t e = smem_limit_once(thin_gate_up_kernel<V>, kSmemBudget + 1024, done);
     if (e != cudaSuccess) return e;
     return launch_pdl(thin_gate_up_kernel<V>, dim3(num_sms), dim3(threads_for(g, 2)), g.smem, s,
                       x, perm, k, H, I, g.R, Wg, Wu, plan.units, plan.wslot, plan.hdr, h, g.stage,
@@ -776,8 +761,8 @@ template <int V>
 cudaError_t launch_d(const __nv_bfloat16* h, int H, int I, const __nv_bfloat16* Wd,
                      const Plan& plan, const Geometry& g, __nv_bfloat16* y, int num_sms,
                      cudaStream_t s) {
-    static int done[64];
-    cudaError_t e = ensure_smem(thin_down_kernel<V>, done);
+    static std::atomic<int> done[kMaxDevices];
+    cudaError_t e = smem_limit_once(thin_down_kernel<V>, kSmemBudget + 1024, done);
     if (e != cudaSuccess) return e;
     return launch_pdl(thin_down_kernel<V>, dim3(num_sms), dim3(threads_for(g, 1)), g.smem, s, h,
                       H, I, g.R, Wd, plan.units, plan.wslot, plan.hdr, y, g.stage, g.slots, g.act);

@@ -27,7 +27,6 @@
 // next item's stream.  Every wait is bounded; on expiry the kernel records
 // MOE_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
-#include <mutex>
 
 #include "moe_internal.cuh"
 #include "ptx.cuh"
@@ -252,14 +251,8 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
 
 template <bool kGated>
 cudaError_t set_smem_attr() {
-    static cudaError_t err = cudaErrorUnknown;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute(thin_mma_kernel<kGated>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   Cfg<kGated>::kSmemBytes);
-    });
-    return err;
+    static std::atomic<int> done[kMaxDevices];
+    return smem_limit_once(thin_mma_kernel<kGated>, Cfg<kGated>::kSmemBytes, done);
 }
 
 }  // namespace
