@@ -144,10 +144,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         int rounds[STAGES];
         for (int s = 0; s < STAGES; ++s) rounds[s] = -1;
         bool ok = true;
+        // Each item's tile is loaded one item ahead (its latency is hidden).
+        FatTile ft_next = {};
+        if (cluster < total) ft_next = args.tiles[2 * (cluster / args.n_blocks_n) + (int)rank];
         for (int w = cluster; ok && w < total; w += n_clusters) {
-            const int pair = w / args.n_blocks_n;
             const int nt = w % args.n_blocks_n;
-            const FatTile ft = args.tiles[2 * pair + (int)rank];
+            const FatTile ft = ft_next;
+            if (w + n_clusters < total)
+                ft_next = args.tiles[2 * ((w + n_clusters) / args.n_blocks_n) + (int)rank];
             const int brow = weight_block(args.wslot, ft.expert) * args.b_rows_per_expert +
                              nt * (kGated ? BM : BN_MMA) +
                              (int)rank * args.b_half_rows;
@@ -236,7 +240,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         const int row = ew * 32 + lane;
         const uint32_t tempty0 = mapa_shared(tempty_bar(0), 0);
         int it = 0;
+        FatTile ft_next = {};
+        if (cluster < total) ft_next = args.tiles[2 * (cluster / args.n_blocks_n) + (int)rank];
         for (int w = cluster; w < total; w += n_clusters, ++it) {
+            const FatTile ft = ft_next;
+            if (w + n_clusters < total)
+                ft_next = args.tiles[2 * ((w + n_clusters) / args.n_blocks_n) + (int)rank];
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)((it >> 1) & 1);
             if (*abort_flag || !mbar_wait(tfull_bar(acc), acc_phase)) {
@@ -245,9 +254,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 break;
             }
             fence_after();
-            const int pair = w / args.n_blocks_n;
             const int nt = w % args.n_blocks_n;
-            const FatTile ft = args.tiles[2 * pair + (int)rank];
             const bool valid = row < ft.rows;
             __nv_bfloat16* dst = args.out + (int64_t)(ft.row0 + row) * args.ld_out +
                                  (int64_t)nt * args.bn_out;

@@ -124,8 +124,12 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
         int pending[C::kStages];
         for (int s = 0; s < C::kStages; ++s) pending[s] = -1;
         bool ok = true;
+        // Each item's tile is loaded one item ahead (its latency is hidden).
+        FatTile ft_next = {};
+        if ((int)blockIdx.x < total) ft_next = args.tiles[blockIdx.x / args.n_blocks];
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-            const FatTile ft = args.tiles[t / args.n_blocks];
+            const FatTile ft = ft_next;
+            if (t + (int)gridDim.x < total) ft_next = args.tiles[(t + gridDim.x) / args.n_blocks];
             const int wrow = weight_block(args.wslot, ft.expert) * args.w_rows_per_expert +
                              (t % args.n_blocks) * BM;
             for (int kb = 0; kb < args.k_blocks; ++kb) {
@@ -205,7 +209,11 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
         // ---------------- epilogue ----------------
         const int ew = warp - 4;   // TMEM lanes (weight rows) 32*ew .. 32*ew+31
         int it = 0;
+        FatTile ft_next = {};
+        if ((int)blockIdx.x < total) ft_next = args.tiles[blockIdx.x / args.n_blocks];
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+            const FatTile ft = ft_next;
+            if (t + (int)gridDim.x < total) ft_next = args.tiles[(t + gridDim.x) / args.n_blocks];
             const int acc = it & 1;
             if (*abort_flag || !mbar_wait(tfull_bar(acc), (uint32_t)((it >> 1) & 1))) {
                 *abort_flag = 1;
@@ -213,7 +221,6 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
                 break;
             }
             fence_after();
-            const FatTile ft = args.tiles[t / args.n_blocks];
             const int col = (t % args.n_blocks) * BM + ew * 32 + lane;
             __nv_bfloat16* dst = args.out + (int64_t)ft.row0 * args.ld_out + col;
             const uint32_t taddr =
