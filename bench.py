@@ -58,6 +58,18 @@ def measured_traffic(kernel: str):
     return None
 
 
+def receipts(moe, layer):
+    """sha256 (first 16 hex digits) of the library that ran and of the step's
+    inputs, so a result can be matched to the exact build and data."""
+    import hashlib
+    with open(moe.LIB_PATH, "rb") as f:
+        lib = hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    h.update(layer.x_cpu.view(torch.int16).numpy().tobytes())
+    h.update(layer.logits_cpu[0].numpy().tobytes())
+    return {"libmoe_sha256_16": lib, "inputs_sha256_16": h.hexdigest()[:16]}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -749,6 +761,7 @@ def run_gpu(args):
             "decode_sweep_4_layers": sweep,
             "offload": offload,
             "peaks": peaks,
+            "receipts": receipts(moe, layer),
         }
         print(json.dumps(line), flush=True)
 

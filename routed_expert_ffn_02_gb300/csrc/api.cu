@@ -6,6 +6,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "moe_internal.cuh"
 
 using namespace moe;
@@ -248,6 +250,15 @@ cudaError_t mark(cudaEvent_t* ev, int i, cudaStream_t s) {
     return (ev && ev[i]) ? cudaEventRecord(ev[i], s) : cudaSuccess;
 }
 
+// NVTX range around the host-side launch of one stage (profilers attribute
+// the stage's kernels to it; without a profiler attached it costs a check).
+struct Nvtx {
+    explicit Nvtx(const char* name) { nvtxRangePushA(name); }
+    ~Nvtx() { nvtxRangePop(); }
+    Nvtx(const Nvtx&) = delete;
+    Nvtx& operator=(const Nvtx&) = delete;
+};
+
 // Expert stage shared by moe_expert_ffn and moe_forward.  `fat_bound` is an
 // upper bound of any expert's count (no GEMM launch when it is below the
 // threshold; it also sizes the streaming kernels' activation buffers).
@@ -261,28 +272,40 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
     const ExpertKernels kn = expert_kernels(sh, fat_bound);
     const int64_t ra = rows_alloc(P);
     const int E = sh->E, H = sh->H, I = sh->I, sms = dev.num_sms;
-    if (kn.gather())
+    if (kn.gather()) {
+        const Nvtx r("moe.gather");
         CUDA_TRY(launch_gather(x, perm, sh->k, H, plan, x_sorted, sms, s), "gather");
+    }
     CUDA_TRY(mark(ev, kEvGather, s), "cudaEventRecord");
-    if (kn.fat)
+    if (kn.fat) {
+        const Nvtx r("moe.gemm_gate_up");
         CUDA_TRY(launch_gemm_gate_up(x_sorted, ra, Wg, Wu, E, H, I, plan, h, sms, s),
                  "grouped GEMM gate/up");
+    }
     CUDA_TRY(mark(ev, kEvGemmGateUp, s), "cudaEventRecord");
-    if (kn.units)
-        CUDA_TRY(launch_thin_gate_up(x, perm, sh->k, H, I, Wg, Wu, plan, fat_bound, h, sms, s),
-                 "thin gate/up");
-    if (kn.mma)
-        CUDA_TRY(launch_thin_mma_gate_up(x_sorted, ra, Wg, Wu, E, H, I, plan, h, sms, s),
-                 "thin gate/up (tensor cores)");
+    {
+        const Nvtx r("moe.thin_gate_up");
+        if (kn.units)
+            CUDA_TRY(launch_thin_gate_up(x, perm, sh->k, H, I, Wg, Wu, plan, fat_bound, h, sms, s),
+                     "thin gate/up");
+        if (kn.mma)
+            CUDA_TRY(launch_thin_mma_gate_up(x_sorted, ra, Wg, Wu, E, H, I, plan, h, sms, s),
+                     "thin gate/up (tensor cores)");
+    }
     CUDA_TRY(mark(ev, kEvThinGateUp, s), "cudaEventRecord");
-    if (kn.fat)
+    if (kn.fat) {
+        const Nvtx r("moe.gemm_down");
         CUDA_TRY(launch_gemm_down(h, ra, Wd, E, H, I, plan, y, sms, s), "grouped GEMM down");
+    }
     CUDA_TRY(mark(ev, kEvGemmDown, s), "cudaEventRecord");
-    if (kn.units)
-        CUDA_TRY(launch_thin_down(h, H, I, Wd, plan, fat_bound, y, sms, s), "thin down");
-    if (kn.mma)
-        CUDA_TRY(launch_thin_mma_down(h, ra, Wd, E, H, I, plan, y, sms, s),
-                 "thin down (tensor cores)");
+    {
+        const Nvtx r("moe.thin_down");
+        if (kn.units)
+            CUDA_TRY(launch_thin_down(h, H, I, Wd, plan, fat_bound, y, sms, s), "thin down");
+        if (kn.mma)
+            CUDA_TRY(launch_thin_mma_down(h, ra, Wd, E, H, I, plan, y, sms, s),
+                     "thin down (tensor cores)");
+    }
     CUDA_TRY(mark(ev, kEvThinDown, s), "cudaEventRecord");
     return MOE_OK;
 }
@@ -423,8 +446,12 @@ static moe_status forward_impl(const moe_shape* shape, const float* logits, cons
     const PdlScope pdl((int64_t)T * k <= kPermChunk);
     int32_t* idx = topk_idx ? topk_idx : b.idx;
     float* g = gates ? gates : b.gates;
+    const Nvtx range("moe_forward");
     CUDA_TRY(mark(ev, kEvStart, s), "cudaEventRecord");
-    CUDA_TRY(launch_route(logits, T, E, k, idx, g, s), "route");
+    {
+        const Nvtx r("moe.route");
+        CUDA_TRY(launch_route(logits, T, E, k, idx, g, s), "route");
+    }
     CUDA_TRY(mark(ev, kEvRoute, s), "cudaEventRecord");
     Plan plan = make_plan(shape, b.tiles, b.units, b.mma_tiles, b.hdr);
     if (wslot) {
@@ -433,8 +460,11 @@ static moe_status forward_impl(const moe_shape* shape, const float* logits, cons
     }
     const int64_t P = (int64_t)T * k;
     const int64_t nch = (P + kPermChunk - 1) / kPermChunk;
-    CUDA_TRY(launch_permute(idx, T, E, k, b.counts, b.offsets, b.perm, b.inv_perm, b.chunk,
-                            b.chunk + nch * E, b.hdr, &plan, s), "permute");
+    {
+        const Nvtx r("moe.permute");
+        CUDA_TRY(launch_permute(idx, T, E, k, b.counts, b.offsets, b.perm, b.inv_perm, b.chunk,
+                                b.chunk + nch * E, b.hdr, &plan, s), "permute");
+    }
     CUDA_TRY(mark(ev, kEvPermute, s), "cudaEventRecord");
     // The router sends a token to k distinct experts, so no expert holds more
     // than T slots.  x_sorted is dead once the gate/up GEMM is done, so
@@ -443,8 +473,11 @@ static moe_status forward_impl(const moe_shape* shape, const float* logits, cons
                      (const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
                      (const __nv_bfloat16*)W_down, b.xy, b.h, b.xy, plan, T, s, ev);
     if (st != MOE_OK) return st;
-    CUDA_TRY(launch_combine(b.xy, b.inv_perm, g, T, k, shape->H, (__nv_bfloat16*)out,
-                            dev.num_sms, s), "combine");
+    {
+        const Nvtx r("moe.combine");
+        CUDA_TRY(launch_combine(b.xy, b.inv_perm, g, T, k, shape->H, (__nv_bfloat16*)out,
+                                dev.num_sms, s), "combine");
+    }
     CUDA_TRY(mark(ev, kEvCombine, s), "cudaEventRecord");
     return ok();
 }
