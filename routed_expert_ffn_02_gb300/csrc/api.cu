@@ -141,9 +141,9 @@ ExpertKernels expert_kernels(const moe_shape* sh, int64_t fat_bound) {
     return k;
 }
 
-Plan make_plan(const moe_shape* sh, FatTile* tiles, ThinUnit* units, FatTile* mma_tiles,
-               WsHeader* hdr) {
-    return Plan{tiles, units, mma_tiles, hdr, sh->fat_threshold,
+Plan make_plan(const moe_shape* sh, FatTile* tiles, FatTile* solo_tiles, ThinUnit* units,
+               FatTile* mma_tiles, WsHeader* hdr) {
+    return Plan{tiles, solo_tiles, units, mma_tiles, hdr, sh->fat_threshold,
                 thin_unit_tokens(sh->H, sh->I), thin_mma_min(sh), nullptr, sh->E};
 }
 
@@ -166,6 +166,7 @@ int64_t rows_alloc(int64_t P) { return std::max<int64_t>(P, kTileM); }
 struct FfnBufs {
     WsHeader* hdr;
     FatTile* tiles;
+    FatTile* solo_tiles;
     ThinUnit* units;
     FatTile* mma_tiles;
     __nv_bfloat16* x_sorted;
@@ -177,6 +178,7 @@ struct FwdBufs {
     int32_t *idx, *counts, *offsets, *perm, *inv_perm, *chunk;
     float* gates;
     FatTile* tiles;
+    FatTile* solo_tiles;
     ThinUnit* units;
     FatTile* mma_tiles;
     __nv_bfloat16* xy;   // x_sorted, later reused for y_sorted
@@ -188,6 +190,7 @@ size_t carve_ffn(const moe_shape* sh, void* ws, FfnBufs* b) {
     Carver c(ws);
     b->hdr = c.take<WsHeader>(1);
     b->tiles = c.take<FatTile>((size_t)max_fat_tiles(P, sh->E));
+    b->solo_tiles = c.take<FatTile>((size_t)sh->E);
     b->units = c.take<ThinUnit>((size_t)max_thin_units(sh->E, thin_unit_tokens(sh->H, sh->I)));
     b->mma_tiles = c.take<FatTile>((size_t)sh->E);
     b->x_sorted = c.take<__nv_bfloat16>((size_t)(rows_alloc(P) * sh->H));
@@ -207,6 +210,7 @@ size_t carve_fwd(const moe_shape* sh, void* ws, FwdBufs* b) {
     b->inv_perm = c.take<int32_t>((size_t)P);
     b->chunk = c.take<int32_t>(permute_scratch_ints(P, sh->E));
     b->tiles = c.take<FatTile>((size_t)max_fat_tiles(P, sh->E));
+    b->solo_tiles = c.take<FatTile>((size_t)sh->E);
     b->units = c.take<ThinUnit>((size_t)max_thin_units(sh->E, thin_unit_tokens(sh->H, sh->I)));
     b->mma_tiles = c.take<FatTile>((size_t)sh->E);
     b->xy = c.take<__nv_bfloat16>((size_t)(rows_alloc(P) * sh->H));
@@ -281,6 +285,8 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
         const Nvtx r("moe.gemm_gate_up");
         CUDA_TRY(launch_gemm_gate_up(x_sorted, ra, Wg, Wu, E, H, I, plan, h, sms, s),
                  "grouped GEMM gate/up");
+        CUDA_TRY(launch_gemm_solo_gate_up(x_sorted, ra, Wg, Wu, H, I, plan, h, sms, s),
+                 "grouped GEMM gate/up (solo tiles)");
     }
     CUDA_TRY(mark(ev, kEvGemmGateUp, s), "cudaEventRecord");
     {
@@ -296,6 +302,8 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
     if (kn.fat) {
         const Nvtx r("moe.gemm_down");
         CUDA_TRY(launch_gemm_down(h, ra, Wd, E, H, I, plan, y, sms, s), "grouped GEMM down");
+        CUDA_TRY(launch_gemm_solo_down(h, ra, Wd, H, I, plan, y, sms, s),
+                 "grouped GEMM down (solo tiles)");
     }
     CUDA_TRY(mark(ev, kEvGemmDown, s), "cudaEventRecord");
     {
@@ -392,7 +400,7 @@ moe_status moe_expert_ffn(const moe_shape* shape, const moe_bf16* x, const int32
     DeviceInfo dev;
     if ((st = device_info(&dev)) != MOE_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    const Plan plan = make_plan(shape, b.tiles, b.units, b.mma_tiles, b.hdr);
+    const Plan plan = make_plan(shape, b.tiles, b.solo_tiles, b.units, b.mma_tiles, b.hdr);
     const PdlScope pdl((int64_t)shape->T * shape->k <= kPermChunk);
     CUDA_TRY(launch_plan(counts, offsets, shape->E, plan, s), "plan");
     st = run_experts(shape, dev, (const __nv_bfloat16*)x, perm, offsets, counts,
@@ -453,7 +461,7 @@ static moe_status forward_impl(const moe_shape* shape, const float* logits, cons
         CUDA_TRY(launch_route(logits, T, E, k, idx, g, s), "route");
     }
     CUDA_TRY(mark(ev, kEvRoute, s), "cudaEventRecord");
-    Plan plan = make_plan(shape, b.tiles, b.units, b.mma_tiles, b.hdr);
+    Plan plan = make_plan(shape, b.tiles, b.solo_tiles, b.units, b.mma_tiles, b.hdr);
     if (wslot) {
         plan.wslot = wslot;
         plan.n_wblocks = n_wblocks;
@@ -523,7 +531,7 @@ int32_t moe_forward_launches(const moe_shape* shape) {
     n += (P <= kPermChunk) ? 1 : 3;                  // route lists (+ planner)
     const ExpertKernels kn = expert_kernels(shape, shape->T);
     if (kn.gather()) n += 1;
-    if (kn.fat) n += 2;                              // grouped GEMMs
+    if (kn.fat) n += 4;                              // grouped GEMMs (pairs, solo tiles)
     if (kn.units) n += 2;                            // CUDA-core streaming
     if (kn.mma) n += 2;                              // tensor-core streaming
     n += 1;                                          // combine

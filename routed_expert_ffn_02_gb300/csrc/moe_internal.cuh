@@ -28,7 +28,8 @@ struct WsHeader {
     int32_t n_thin;        // work units on the weight-streaming path
     int32_t thin_weight;   // sum of thin_unit_cost over those units
     int32_t n_thin_mma;    // thin experts on the tensor-core streaming kernel
-    int32_t reserved[59];
+    int32_t n_solo;        // fat experts' leftover 128-row tiles (one-CTA GEMM)
+    int32_t reserved[58];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -110,7 +111,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // its weights through the tensor cores (one FatTile of <= kThinMaxTokens rows
 // in mma_tiles); the others take the CUDA-core streaming kernel (units).
 struct Plan {
-    FatTile* tiles;      // [max_fat_tiles(P, E)]
+    FatTile* tiles;      // [max_fat_tiles(P, E)], in pairs of one expert
+    FatTile* solo_tiles; // [E]: an expert's last tile when its tile count is odd
     ThinUnit* units;     // [max_thin_units(E, unit_tokens)], expert-major
     FatTile* mma_tiles;  // [E]
     WsHeader* hdr;
@@ -188,6 +190,16 @@ cudaError_t launch_thin_mma_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_
 cudaError_t launch_thin_mma_down(const __nv_bfloat16* h, int64_t rows_alloc,
                                  const __nv_bfloat16* Wd, int E, int H, int I, const Plan& plan,
                                  __nv_bfloat16* y_sorted, int num_sms, cudaStream_t s);
+
+// One-CTA grouped GEMMs (tcgen05 cta_group::1, 128 x 256 tiles) over
+// plan.solo_tiles, the same products as the pair GEMMs below.
+cudaError_t launch_gemm_solo_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_alloc,
+                                     const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int H,
+                                     int I, const Plan& plan, __nv_bfloat16* h, int num_sms,
+                                     cudaStream_t s);
+cudaError_t launch_gemm_solo_down(const __nv_bfloat16* h, int64_t rows_alloc,
+                                  const __nv_bfloat16* Wd, int H, int I, const Plan& plan,
+                                  __nv_bfloat16* y_sorted, int num_sms, cudaStream_t s);
 
 // Grouped GEMMs on tcgen05.  gate_up: h = silu(A Wg^T) * (A Wu^T) for the
 // fat tiles, A = x_sorted [rows_alloc, H].  down: y = h Wd^T, A = h.

@@ -84,13 +84,14 @@ __device__ void block_plan(const int* cnt, const int* off, int E, const Plan& pl
     auto is_fat = [&](int c) { return c > 0 && c >= thr; };
     auto is_mma = [&](int c) { return c > 0 && c < thr && c >= mma_min; };
     auto is_unit = [&](int c) { return c > 0 && c < thr && c < mma_min; };
-    // A fat expert's 128-row tiles come in pairs (a 256-row block of its
-    // slots: tiles 2q and 2q+1 cover rows [256q, 256q+128) and
-    // [256q+128, 256q+256)), so the grouped GEMM can run each pair on a CTA
-    // pair; the second tile of a ragged block may hold 0 rows.
+    // A fat expert's 128-row tiles come in pairs (tiles 2q and 2q+1 cover
+    // rows [256q, 256q+128) and [256q+128, 256q+256)), so the grouped GEMM
+    // can run each pair on a CTA pair; when the expert has an odd number of
+    // tiles its last one is a solo tile for the one-CTA GEMM.
+    auto n_tiles_of = [](int c) { return (c + kTileM - 1) / kTileM; };
     for (int e = threadIdx.x; e < E; e += NT) {
         const int c = cnt[e];
-        ta[e] = is_fat(c) ? 2 * ((c + 2 * kTileM - 1) / (2 * kTileM)) : 0;
+        ta[e] = is_fat(c) ? (n_tiles_of(c) & ~1) : 0;
         tb[e] = is_mma(c) ? 1 : 0;
     }
     __syncthreads();
@@ -99,12 +100,12 @@ __device__ void block_plan(const int* cnt, const int* off, int E, const Plan& pl
     for (int e = threadIdx.x; e < E; e += NT) {
         const int c = cnt[e];
         if (is_fat(c)) {
-            const int nt = 2 * ((c + 2 * kTileM - 1) / (2 * kTileM));
+            const int nt = n_tiles_of(c) & ~1;
             for (int i = 0; i < nt; ++i) {
                 FatTile ft;
                 ft.expert = e;
                 ft.row0 = off[e] + i * kTileM;
-                ft.rows = max(0, min(kTileM, c - i * kTileM));
+                ft.rows = min(kTileM, c - i * kTileM);
                 ft.pad = 0;
                 plan.tiles[ta[e] + i] = ft;
             }
@@ -115,6 +116,26 @@ __device__ void block_plan(const int* cnt, const int* off, int E, const Plan& pl
             ft.rows = c;
             ft.pad = 0;
             plan.mma_tiles[tb[e]] = ft;
+        }
+    }
+    __syncthreads();
+    // solo tiles: the last tile of fat experts with an odd tile count
+    for (int e = threadIdx.x; e < E; e += NT) {
+        const int c = cnt[e];
+        ta[e] = (is_fat(c) && (n_tiles_of(c) & 1)) ? 1 : 0;
+    }
+    __syncthreads();
+    const int n_solo = block_exclusive_scan<NT>(ta, E, ws);
+    for (int e = threadIdx.x; e < E; e += NT) {
+        const int c = cnt[e];
+        if (is_fat(c) && (n_tiles_of(c) & 1)) {
+            const int i = n_tiles_of(c) - 1;
+            FatTile ft;
+            ft.expert = e;
+            ft.row0 = off[e] + i * kTileM;
+            ft.rows = c - i * kTileM;
+            ft.pad = 0;
+            plan.solo_tiles[ta[e]] = ft;
         }
     }
     __syncthreads();
@@ -150,6 +171,7 @@ __device__ void block_plan(const int* cnt, const int* off, int E, const Plan& pl
         plan.hdr->n_thin = n_units;
         plan.hdr->thin_weight = weight;
         plan.hdr->n_thin_mma = n_mma;
+        plan.hdr->n_solo = n_solo;
     }
 }
 
@@ -358,12 +380,13 @@ plan_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ offs
     block_plan<1024>(cnt, off, E, plan, ta, tb, ws);
 }
 
-// x_sorted[p] = x[perm[p] / k] for the rows of the fat tiles and of the
-// tensor-core streaming tiles; one warp per row, 16-byte vectors.
+// x_sorted[p] = x[perm[p] / k] for the rows of the fat tiles (paired and
+// solo) and of the tensor-core streaming tiles; one warp per row, 16-byte
+// vectors.
 __global__ void __launch_bounds__(256)
 gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
               int k, int H, const FatTile* __restrict__ tiles,
-              const FatTile* __restrict__ mma_tiles,
+              const FatTile* __restrict__ solo_tiles, const FatTile* __restrict__ mma_tiles,
               const WsHeader* __restrict__ hdr, uint4* __restrict__ x_sorted) {
     ptx::grid_dep_wait();
     ptx::grid_dep_launch();
@@ -371,12 +394,22 @@ gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int64_t fat_rows = (int64_t)hdr->n_fat_tiles * kTileM;
-    const int64_t rows = fat_rows + (int64_t)hdr->n_thin_mma * kThinMaxTokens;
+    const int64_t solo_rows = fat_rows + (int64_t)hdr->n_solo * kTileM;
+    const int64_t rows = solo_rows + (int64_t)hdr->n_thin_mma * kThinMaxTokens;
     const int vec = H / 8;
     for (int64_t r = warp; r < rows; r += nwarps) {
-        const FatTile ft = r < fat_rows ? tiles[r / kTileM]
-                                        : mma_tiles[(r - fat_rows) / kThinMaxTokens];
-        const int i = r < fat_rows ? (int)(r % kTileM) : (int)((r - fat_rows) % kThinMaxTokens);
+        FatTile ft;
+        int i;
+        if (r < fat_rows) {
+            ft = tiles[r / kTileM];
+            i = (int)(r % kTileM);
+        } else if (r < solo_rows) {
+            ft = solo_tiles[(r - fat_rows) / kTileM];
+            i = (int)((r - fat_rows) % kTileM);
+        } else {
+            ft = mma_tiles[(r - solo_rows) / kThinMaxTokens];
+            i = (int)((r - solo_rows) % kThinMaxTokens);
+        }
         if (i >= ft.rows) continue;
         const int64_t p = ft.row0 + i;
         const int64_t t = perm[p] / k;
@@ -427,8 +460,8 @@ cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* perm, int k,
                           int H, const Plan& plan, __nv_bfloat16* x_sorted,
                           int num_sms, cudaStream_t s) {
     return launch_pdl(gather_kernel, dim3(num_sms * 8), dim3(256), 0, s,
-                      reinterpret_cast<const uint4*>(x), perm, k, H, plan.tiles, plan.mma_tiles,
-                      plan.hdr, reinterpret_cast<uint4*>(x_sorted));
+                      reinterpret_cast<const uint4*>(x), perm, k, H, plan.tiles, plan.solo_tiles,
+                      plan.mma_tiles, plan.hdr, reinterpret_cast<uint4*>(x_sorted));
 }
 
 }  // namespace moe

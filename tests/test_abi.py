@@ -144,9 +144,10 @@ def test_forward_launch_count(moe):
     assert moe.forward_launches(S(3, 384, 8, 4096, 2048)) == 6       # 24 x 16 = 384: tensor cores
     assert moe.forward_launches(S(1, 384, 8, 4096, 2048, thin_mma_min=1)) == 6
     assert moe.forward_launches(S(4, 384, 8, 4096, 2048, thin_mma_min=33)) == 5
-    assert moe.forward_launches(S(16384, 384, 8, 4096, 2048)) == 10
-    assert moe.forward_launches(S(16384, 384, 8, 4096, 2048, thin_mma_min=8)) == 12
-    assert moe.forward_launches(S(16384, 384, 8, 4096, 2048, fat_threshold=0)) == 8
+    # fat experts: pair GEMMs and solo-tile GEMMs for gate/up and down
+    assert moe.forward_launches(S(16384, 384, 8, 4096, 2048)) == 12
+    assert moe.forward_launches(S(16384, 384, 8, 4096, 2048, thin_mma_min=8)) == 14
+    assert moe.forward_launches(S(16384, 384, 8, 4096, 2048, fat_threshold=0)) == 10
     assert moe.forward_launches(S(0, 384, 8, 4096, 2048)) == 0
 
 
