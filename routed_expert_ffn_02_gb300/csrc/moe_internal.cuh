@@ -112,7 +112,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // in mma_tiles); the others take the CUDA-core streaming kernel (units).
 struct Plan {
     FatTile* tiles;      // [max_fat_tiles(P, E)], in pairs of one expert
-    FatTile* solo_tiles; // [E]: an expert's last tile when its tile count is odd
+    FatTile* solo_tiles; // [E]: experts with a single tile (at most kTileM slots)
     ThinUnit* units;     // [max_thin_units(E, unit_tokens)], expert-major
     FatTile* mma_tiles;  // [E]
     WsHeader* hdr;

@@ -86,12 +86,16 @@ __device__ void block_plan(const int* cnt, const int* off, int E, const Plan& pl
     auto is_unit = [&](int c) { return c > 0 && c < thr && c < mma_min; };
     // A fat expert's 128-row tiles come in pairs (tiles 2q and 2q+1 cover
     // rows [256q, 256q+128) and [256q+128, 256q+256)), so the grouped GEMM
-    // can run each pair on a CTA pair; when the expert has an odd number of
-    // tiles its last one is a solo tile for the one-CTA GEMM.
+    // can run each pair on a CTA pair.  An expert with a single tile (at most
+    // 128 slots) is a solo tile for the one-CTA GEMM; an expert with an odd
+    // number of tiles above one pads its last pair with an empty tile (a solo
+    // tile there would read the expert's weights from DRAM a second time).
     auto n_tiles_of = [](int c) { return (c + kTileM - 1) / kTileM; };
+    auto is_solo = [&](int c) { return is_fat(c) && n_tiles_of(c) == 1; };
+    auto paired_of = [&](int c) { return (is_fat(c) && !is_solo(c)) ? (n_tiles_of(c) + 1) & ~1 : 0; };
     for (int e = threadIdx.x; e < E; e += NT) {
         const int c = cnt[e];
-        ta[e] = is_fat(c) ? (n_tiles_of(c) & ~1) : 0;
+        ta[e] = paired_of(c);
         tb[e] = is_mma(c) ? 1 : 0;
     }
     __syncthreads();
@@ -99,13 +103,13 @@ __device__ void block_plan(const int* cnt, const int* off, int E, const Plan& pl
     const int n_mma = block_exclusive_scan<NT>(tb, E, ws);
     for (int e = threadIdx.x; e < E; e += NT) {
         const int c = cnt[e];
-        if (is_fat(c)) {
-            const int nt = n_tiles_of(c) & ~1;
+        if (paired_of(c) > 0) {
+            const int nt = paired_of(c);
             for (int i = 0; i < nt; ++i) {
                 FatTile ft;
                 ft.expert = e;
                 ft.row0 = off[e] + i * kTileM;
-                ft.rows = min(kTileM, c - i * kTileM);
+                ft.rows = max(0, min(kTileM, c - i * kTileM));
                 ft.pad = 0;
                 plan.tiles[ta[e] + i] = ft;
             }
@@ -119,21 +123,17 @@ __device__ void block_plan(const int* cnt, const int* off, int E, const Plan& pl
         }
     }
     __syncthreads();
-    // solo tiles: the last tile of fat experts with an odd tile count
-    for (int e = threadIdx.x; e < E; e += NT) {
-        const int c = cnt[e];
-        ta[e] = (is_fat(c) && (n_tiles_of(c) & 1)) ? 1 : 0;
-    }
+    // solo tiles: fat experts with a single tile
+    for (int e = threadIdx.x; e < E; e += NT) ta[e] = is_solo(cnt[e]) ? 1 : 0;
     __syncthreads();
     const int n_solo = block_exclusive_scan<NT>(ta, E, ws);
     for (int e = threadIdx.x; e < E; e += NT) {
         const int c = cnt[e];
-        if (is_fat(c) && (n_tiles_of(c) & 1)) {
-            const int i = n_tiles_of(c) - 1;
+        if (is_solo(c)) {
             FatTile ft;
             ft.expert = e;
-            ft.row0 = off[e] + i * kTileM;
-            ft.rows = c - i * kTileM;
+            ft.row0 = off[e];
+            ft.rows = c;
             ft.pad = 0;
             plan.solo_tiles[ta[e]] = ft;
         }
