@@ -267,15 +267,14 @@ struct Nvtx {
 // upper bound of any expert's count (no GEMM launch when it is below the
 // threshold; it also sizes the streaming kernels' activation buffers).
 moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bfloat16* x,
-                       const int32_t* perm, const int32_t* offsets, const int32_t* counts,
-                       const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
+                       const int32_t* perm, const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
                        const __nv_bfloat16* Wd, __nv_bfloat16* x_sorted,
                        __nv_bfloat16* h, __nv_bfloat16* y, const Plan& plan,
                        int64_t fat_bound, cudaStream_t s, cudaEvent_t* ev) {
     const int64_t P = (int64_t)sh->T * sh->k;
     const ExpertKernels kn = expert_kernels(sh, fat_bound);
     const int64_t ra = rows_alloc(P);
-    const int E = sh->E, H = sh->H, I = sh->I, sms = dev.num_sms;
+    const int H = sh->H, I = sh->I, sms = dev.num_sms;
     if (kn.gather()) {
         const Nvtx r("moe.gather");
         CUDA_TRY(launch_gather(x, perm, sh->k, H, plan, x_sorted, sms, s), "gather");
@@ -283,7 +282,7 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
     CUDA_TRY(mark(ev, kEvGather, s), "cudaEventRecord");
     if (kn.fat) {
         const Nvtx r("moe.gemm_gate_up");
-        CUDA_TRY(launch_gemm_gate_up(x_sorted, ra, Wg, Wu, E, H, I, plan, h, sms, s),
+        CUDA_TRY(launch_gemm_gate_up(x_sorted, ra, Wg, Wu, H, I, plan, h, sms, s),
                  "grouped GEMM gate/up");
         CUDA_TRY(launch_gemm_solo_gate_up(x_sorted, ra, Wg, Wu, H, I, plan, h, sms, s),
                  "grouped GEMM gate/up (solo tiles)");
@@ -295,13 +294,13 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
             CUDA_TRY(launch_thin_gate_up(x, perm, sh->k, H, I, Wg, Wu, plan, fat_bound, h, sms, s),
                      "thin gate/up");
         if (kn.mma)
-            CUDA_TRY(launch_thin_mma_gate_up(x_sorted, ra, Wg, Wu, E, H, I, plan, h, sms, s),
+            CUDA_TRY(launch_thin_mma_gate_up(x_sorted, ra, Wg, Wu, H, I, plan, h, sms, s),
                      "thin gate/up (tensor cores)");
     }
     CUDA_TRY(mark(ev, kEvThinGateUp, s), "cudaEventRecord");
     if (kn.fat) {
         const Nvtx r("moe.gemm_down");
-        CUDA_TRY(launch_gemm_down(h, ra, Wd, E, H, I, plan, y, sms, s), "grouped GEMM down");
+        CUDA_TRY(launch_gemm_down(h, ra, Wd, H, I, plan, y, sms, s), "grouped GEMM down");
         CUDA_TRY(launch_gemm_solo_down(h, ra, Wd, H, I, plan, y, sms, s),
                  "grouped GEMM down (solo tiles)");
     }
@@ -311,7 +310,7 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
         if (kn.units)
             CUDA_TRY(launch_thin_down(h, H, I, Wd, plan, fat_bound, y, sms, s), "thin down");
         if (kn.mma)
-            CUDA_TRY(launch_thin_mma_down(h, ra, Wd, E, H, I, plan, y, sms, s),
+            CUDA_TRY(launch_thin_mma_down(h, ra, Wd, H, I, plan, y, sms, s),
                      "thin down (tensor cores)");
     }
     CUDA_TRY(mark(ev, kEvThinDown, s), "cudaEventRecord");
@@ -403,10 +402,9 @@ moe_status moe_expert_ffn(const moe_shape* shape, const moe_bf16* x, const int32
     const Plan plan = make_plan(shape, b.tiles, b.solo_tiles, b.units, b.mma_tiles, b.hdr);
     const PdlScope pdl((int64_t)shape->T * shape->k <= kPermChunk);
     CUDA_TRY(launch_plan(counts, offsets, shape->E, plan, s), "plan");
-    st = run_experts(shape, dev, (const __nv_bfloat16*)x, perm, offsets, counts,
-                     (const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
-                     (const __nv_bfloat16*)W_down, b.x_sorted, b.h, (__nv_bfloat16*)y_sorted,
-                     plan, (int64_t)shape->T * shape->k, s, nullptr);
+    st = run_experts(shape, dev, (const __nv_bfloat16*)x, perm, (const __nv_bfloat16*)W_gate,
+                     (const __nv_bfloat16*)W_up, (const __nv_bfloat16*)W_down, b.x_sorted, b.h,
+                     (__nv_bfloat16*)y_sorted, plan, (int64_t)shape->T * shape->k, s, nullptr);
     return st == MOE_OK ? ok() : st;
 }
 
@@ -477,9 +475,9 @@ static moe_status forward_impl(const moe_shape* shape, const float* logits, cons
     // The router sends a token to k distinct experts, so no expert holds more
     // than T slots.  x_sorted is dead once the gate/up GEMM is done, so
     // y_sorted reuses its storage.
-    st = run_experts(shape, dev, (const __nv_bfloat16*)x, b.perm, b.offsets, b.counts,
-                     (const __nv_bfloat16*)W_gate, (const __nv_bfloat16*)W_up,
-                     (const __nv_bfloat16*)W_down, b.xy, b.h, b.xy, plan, T, s, ev);
+    st = run_experts(shape, dev, (const __nv_bfloat16*)x, b.perm, (const __nv_bfloat16*)W_gate,
+                     (const __nv_bfloat16*)W_up, (const __nv_bfloat16*)W_down, b.xy, b.h, b.xy,
+                     plan, T, s, ev);
     if (st != MOE_OK) return st;
     {
         const Nvtx r("moe.combine");

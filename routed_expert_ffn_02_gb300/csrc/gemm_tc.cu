@@ -386,9 +386,9 @@ cudaError_t make_tma_map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, ui
 }
 
 cudaError_t launch_gemm_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_alloc,
-                                const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
-                                int E, int H, int I, const Plan& plan,
-                                __nv_bfloat16* h, int num_sms, cudaStream_t s) {
+                                const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int H, int I,
+                                const Plan& plan, __nv_bfloat16* h, int num_sms,
+                                cudaStream_t s) {
     CUtensorMap mA, mG, mU;
     cudaError_t e;
     if ((e = make_tma_map_bf16(&mA, x_sorted, (uint64_t)rows_alloc, (uint64_t)H, BM)) != cudaSuccess) return e;
@@ -414,9 +414,8 @@ cudaError_t launch_gemm_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_allo
 }
 
 cudaError_t launch_gemm_down(const __nv_bfloat16* h, int64_t rows_alloc,
-                             const __nv_bfloat16* Wd, int E, int H, int I,
-                             const Plan& plan, __nv_bfloat16* y_sorted,
-                             int num_sms, cudaStream_t s) {
+                             const __nv_bfloat16* Wd, int H, int I, const Plan& plan,
+                             __nv_bfloat16* y_sorted, int num_sms, cudaStream_t s) {
     CUtensorMap mA, mD;
     cudaError_t e;
     if ((e = make_tma_map_bf16(&mA, h, (uint64_t)rows_alloc, (uint64_t)I, BM)) != cudaSuccess) return e;

@@ -184,11 +184,11 @@ cudaError_t launch_thin_down(const __nv_bfloat16* h, int H, int I, const __nv_bf
 // gate_up: h[rows] = silu(x_sorted[rows] Wg_e^T) * (x_sorted[rows] Wu_e^T);
 // down: y[rows] = h[rows] Wd_e^T.  x_sorted / h hold rows_alloc rows.
 cudaError_t launch_thin_mma_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_alloc,
-                                    const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int E,
-                                    int H, int I, const Plan& plan, __nv_bfloat16* h,
-                                    int num_sms, cudaStream_t s);
+                                    const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int H,
+                                    int I, const Plan& plan, __nv_bfloat16* h, int num_sms,
+                                    cudaStream_t s);
 cudaError_t launch_thin_mma_down(const __nv_bfloat16* h, int64_t rows_alloc,
-                                 const __nv_bfloat16* Wd, int E, int H, int I, const Plan& plan,
+                                 const __nv_bfloat16* Wd, int H, int I, const Plan& plan,
                                  __nv_bfloat16* y_sorted, int num_sms, cudaStream_t s);
 
 // One-CTA grouped GEMMs (tcgen05 cta_group::1, 128 x 256 tiles) over
@@ -204,13 +204,12 @@ cudaError_t launch_gemm_solo_down(const __nv_bfloat16* h, int64_t rows_alloc,
 // Grouped GEMMs on tcgen05.  gate_up: h = silu(A Wg^T) * (A Wu^T) for the
 // fat tiles, A = x_sorted [rows_alloc, H].  down: y = h Wd^T, A = h.
 cudaError_t launch_gemm_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_alloc,
-                                const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
-                                int E, int H, int I, const Plan& plan,
-                                __nv_bfloat16* h, int num_sms, cudaStream_t s);
+                                const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int H, int I,
+                                const Plan& plan, __nv_bfloat16* h, int num_sms,
+                                cudaStream_t s);
 cudaError_t launch_gemm_down(const __nv_bfloat16* h, int64_t rows_alloc,
-                             const __nv_bfloat16* Wd, int E, int H, int I,
-                             const Plan& plan, __nv_bfloat16* y_sorted,
-                             int num_sms, cudaStream_t s);
+                             const __nv_bfloat16* Wd, int H, int I, const Plan& plan,
+                             __nv_bfloat16* y_sorted, int num_sms, cudaStream_t s);
 
 cudaError_t launch_combine(const __nv_bfloat16* y_sorted, const int32_t* inv_perm,
                            const float* gates, int T, int k, int H,

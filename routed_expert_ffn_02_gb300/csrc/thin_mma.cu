@@ -265,9 +265,9 @@ cudaError_t set_smem_attr() {
 }  // namespace
 
 cudaError_t launch_thin_mma_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_alloc,
-                                    const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int E,
-                                    int H, int I, const Plan& plan, __nv_bfloat16* h,
-                                    int num_sms, cudaStream_t s) {
+                                    const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int H,
+                                    int I, const Plan& plan, __nv_bfloat16* h, int num_sms,
+                                    cudaStream_t s) {
     CUtensorMap mX, mG, mU;
     cudaError_t e;
     if ((e = make_tma_map_bf16(&mX, x_sorted, (uint64_t)rows_alloc, (uint64_t)H, BN)) != cudaSuccess) return e;
@@ -289,7 +289,7 @@ cudaError_t launch_thin_mma_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_
 }
 
 cudaError_t launch_thin_mma_down(const __nv_bfloat16* h, int64_t rows_alloc,
-                                 const __nv_bfloat16* Wd, int E, int H, int I, const Plan& plan,
+                                 const __nv_bfloat16* Wd, int H, int I, const Plan& plan,
                                  __nv_bfloat16* y_sorted, int num_sms, cudaStream_t s) {
     CUtensorMap mX, mD;
     cudaError_t e;
