@@ -724,12 +724,15 @@ struct Geometry {
     int R, stage, slots, act, smem;
 };
 
-// act_tokens: most slots any unit can hold here (the activation buffer size).
-Geometry geometry(int row_bytes, int act_row_bytes, int act_tokens) {
+// act_tokens: most slots any unit can hold here (the activation buffer size);
+// pad4: round the buffer up to a multiple of 4 rows (the down kernel's
+// grouped register path reads whole groups of 4; gate/up reads exactly the
+// unit's rows).  Every H, I the library accepts fits kSmemBudget.
+Geometry geometry(int row_bytes, int act_row_bytes, int act_tokens, bool pad4) {
     Geometry g;
     g.R = rows_per_item(row_bytes);
     g.stage = g.R * row_bytes;
-    g.act = ((act_tokens + 3) / 4 * 4) * act_row_bytes;   // groups of 4 read whole groups
+    g.act = (pad4 ? (act_tokens + 3) / 4 * 4 : act_tokens) * act_row_bytes;
     g.slots = (kSmemBudget - g.act) / g.stage;
     if (g.slots > kMaxSlots) g.slots = kMaxSlots;
     if (g.slots < 2) g.slots = 2;
@@ -783,7 +786,11 @@ cudaError_t launch_thin_gate_up(const __nv_bfloat16* x, const int32_t* perm, int
                                 int num_sms, cudaStream_t s) {
     const int act_tokens =
         (int)std::min<int64_t>(plan.unit_tokens, std::max<int64_t>(max_slots, 1));
-    const Geometry g = geometry(2 * H * 2, H * 2, act_tokens);
+    const Geometry g = geometry(2 * H * 2, H * 2, act_tokens, false);
+    if (g.smem > kSmemBudget + 1024) {
+        set_last_error("thin gate/up: H = %d needs %d bytes of shared memory", H, g.smem);
+        return cudaErrorInvalidConfiguration;
+    }
     switch (g.stage == kStageTarget ? H : 0) {
         case 256: return launch_gu<1>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s);
         case 512: return launch_gu<2>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s);
@@ -799,7 +806,11 @@ cudaError_t launch_thin_down(const __nv_bfloat16* h, int H, int I, const __nv_bf
                              int num_sms, cudaStream_t s) {
     const int act_tokens =
         (int)std::min<int64_t>(plan.unit_tokens, std::max<int64_t>(max_slots, 1));
-    const Geometry g = geometry(I * 2, I * 2, act_tokens);
+    const Geometry g = geometry(I * 2, I * 2, act_tokens, true);
+    if (g.smem > kSmemBudget + 1024) {
+        set_last_error("thin down: I = %d needs %d bytes of shared memory", I, g.smem);
+        return cudaErrorInvalidConfiguration;
+    }
     switch (g.stage == kStageTarget ? I : 0) {
         case 256: return launch_d<1>(h, H, I, Wd, plan, g, y_sorted, num_sms, s);
         case 512: return launch_d<2>(h, H, I, Wd, plan, g, y_sorted, num_sms, s);

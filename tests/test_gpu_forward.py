@@ -313,3 +313,23 @@ def test_thin_units_split_at_full_width(moe, mma_min):
     inp = synth.make_layer(s, seed=8)
     inp["logits"] = lg
     _full_check(moe, s, 33, inp, mma_min=mma_min)
+
+
+@pytest.mark.parametrize("T,E,k,H,I", [(64, 1024, 8, 256, 256),     # most experts, top-8
+                                       (40, 4, 2, 16384, 256),      # largest hidden size
+                                       (40, 4, 2, 256, 16384)])     # largest intermediate size
+@pytest.mark.parametrize("thr,mma_min", [(0, 0), (33, MMA_ALL), (33, MMA_NONE)])
+def test_forward_maximum_sizes(moe, T, E, k, H, I, thr, mma_min):
+    """The limits moe.h accepts (E = 1024, H or I = 16384) on each expert
+    kernel: grouped GEMM (thr=0), tensor-core and CUDA-core weight streaming.
+    The max-abs bound was set at the model's magnitudes (H = 4096, I = 2048);
+    with the fixed 0.02 weight scale, pre-activations grow with sqrt(H) and
+    sqrt(I), so the weights are rescaled to keep that variance (one bf16 ulp
+    of an output near 8 is already 0.03).  The oracle reads the same bytes."""
+    s = synth.Shape(T=T, E=E, k=k, H=H, I=I)
+    inp = synth.make_layer(s, seed=T + E, zipf_s=synth.ZIPF_S)
+    gu, d = min(1.0, (4096 / H) ** 0.5), min(1.0, (2048 / I) ** 0.5)
+    inp["Wg"] = (inp["Wg"].float() * gu).to(torch.bfloat16)
+    inp["Wu"] = (inp["Wu"].float() * gu).to(torch.bfloat16)
+    inp["Wd"] = (inp["Wd"].float() * d).to(torch.bfloat16)
+    _full_check(moe, s, thr, inp, mma_min=mma_min)
