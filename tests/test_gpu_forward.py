@@ -333,3 +333,25 @@ def test_forward_maximum_sizes(moe, T, E, k, H, I, thr, mma_min):
     inp["Wu"] = (inp["Wu"].float() * gu).to(torch.bfloat16)
     inp["Wd"] = (inp["Wd"].float() * d).to(torch.bfloat16)
     _full_check(moe, s, thr, inp, mma_min=mma_min)
+
+
+@pytest.mark.parametrize("T", [256, 257])
+def test_route_lists_at_the_small_path_boundary(moe, T):
+    """T*k = 2048 takes the single-block route-list kernel, 2056 the
+    histogram / scan / scatter kernels: both bit-exact, same forward."""
+    s = synth.Shape(T=T, E=64, k=8, H=256, I=256)
+    inp = synth.make_layer(s, seed=T, zipf_s=synth.ZIPF_S)
+    _full_check(moe, s, 32, inp)
+    idx, _ = moe.moe_route(inp["logits"].cuda(), s.k)
+    counts, offsets, perm, inv = moe.moe_permute(idx, s.E)
+    rc, ro, rp, ri = oracle.permute(idx.cpu().numpy(), s.E)
+    assert np.array_equal(counts.cpu().numpy(), rc) and np.array_equal(offsets.cpu().numpy(), ro)
+    assert np.array_equal(perm.cpu().numpy(), rp) and np.array_equal(inv.cpu().numpy(), ri)
+
+
+@pytest.mark.parametrize("thr", [0, 33])
+def test_forward_single_expert(moe, thr):
+    """E = 1, k = 1: every token's gate is 1 and the layer is one dense
+    SwiGLU FFN (GEMM or streaming path)."""
+    s = synth.Shape(T=50, E=1, k=1, H=512, I=256)
+    _full_check(moe, s, thr, synth.make_layer(s, seed=3))

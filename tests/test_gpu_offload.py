@@ -17,7 +17,8 @@ def moe():
     return m
 
 
-@pytest.mark.parametrize("T,E,k,H,I,L,slots", [(64, 16, 2, 512, 256, 5, 2),
+@pytest.mark.parametrize("T,E,k,H,I,L,slots", [(64, 16, 2, 512, 256, 4, 1),
+                                                (64, 16, 2, 512, 256, 5, 2),
                                                 (1024, 32, 8, 2048, 1024, 4, 3),
                                                 (4, 64, 8, 2048, 1024, 3, 8)])
 def test_offload_matches_resident_forward(moe, T, E, k, H, I, L, slots):
