@@ -642,6 +642,15 @@ def run_gpu(args):
         / (peaks["bf16_tflops_sustained"] * 1e12),
         sum(w["bytes"] for n, w in work.items() if not n.startswith("_"))
         / (peaks["hbm_gbs"] * 1e9)) * 1e3
+    # No-overlap bound: each touched expert alone at whichever of the tensor
+    # or HBM roofline binds it (weights once, its rows of x in and y out),
+    # summed over experts, so memory-bound medium and thin experts show.
+    per_expert_ms = 0.0
+    for n_e in counts[counts > 0]:
+        f = 6.0 * int(n_e) * shape.H * shape.I
+        b = 3.0 * shape.H * shape.I * 2 + int(n_e) * shape.H * 2 * 2
+        per_expert_ms += max(f / (peaks["bf16_tflops_sustained"] * 1e12),
+                             b / (peaks["hbm_gbs"] * 1e9)) * 1e3
 
     # end to end through the C ABI with host buffers (moe_forward_host): every
     # step copies its logits and x in from pinned host memory and its output
@@ -751,7 +760,12 @@ def run_gpu(args):
             "layer_roofline": {"ideal_ms": round(layer_ideal_ms, 4),
                                "frac": round(layer_ideal_ms / ms_per_step, 4),
                                "note": "max(all flops / bf16 sustained peak, all algorithmic "
-                                       "bytes / HBM peak) over the whole layer"},
+                                       "bytes / HBM peak) over the whole layer",
+                               "per_expert_ideal_ms": round(per_expert_ms, 4),
+                               "per_expert_frac": round(per_expert_ms / ms_per_step, 4),
+                               "per_expert_note": "sum over touched experts of max(flops / "
+                                                  "bf16 sustained peak, bytes / HBM peak): no "
+                                                  "overlap between experts"},
             "stages": stages,
             "cpu_baseline": cpu,
             "e2e": e2e,
