@@ -780,6 +780,23 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
 
 
+def run_decode_profile(args):
+    """A few eager decode forwards at batch B on the full E=384, H=4096,
+    I=2048 layer, 8 logit sets rotated (so each forward touches new
+    experts); prints mean stage times.  For ncu."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    import routed_expert_ffn_02_gb300 as moe
+    B = args.decode_profile
+    shape = moe.Shape(B, PREFILL.E, PREFILL.k, PREFILL.H, PREFILL.I, FAT_THRESHOLD,
+                      args.thin_mma_min)
+    layer = Layer(moe, shape, dev, n_logit_sets=8)
+    _, stage_ms = time_steps(layer, 8, 3)
+    print(json.dumps({"decode_profile": f"B{B}",
+                      "stage_us": {k: round(1e3 * v, 2) for k, v in stage_ms.items()}}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -801,11 +818,17 @@ def main():
     ap.add_argument("--thin-mma-min", type=int, default=0,
                     help="slots from which a thin expert streams on the tensor cores "
                          "(0: library default; 33: CUDA cores only)")
+    ap.add_argument("--decode-profile", type=int, default=None, metavar="B",
+                    help="only run 8 eager decode forwards at batch B on the full layer "
+                         "(for profilers) and print their stage times")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.decode_profile:
+        run_decode_profile(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
