@@ -125,6 +125,16 @@ int thin_mma_min(const moe_shape* sh) {
     return touched * (sh->I / 128) >= kThinMmaAutoItems ? 1 : kThinMaxTokens + 1;
 }
 
+// Small batches whose touched experts are all thin, on the CUDA-core streaming
+// kernel and in one unit each are routed inside the streaming kernels and
+// combined by the down kernel (see SelfRoute): no router, route-list, planner
+// or combine launch.  A token's k experts are distinct, so no expert holds
+// more than T slots.
+bool self_routed(const moe_shape* sh) {
+    return (int64_t)sh->T * sh->k <= kSelfRouteSlots && sh->T < sh->fat_threshold &&
+           sh->T < thin_mma_min(sh) && sh->T <= thin_unit_tokens(sh->H, sh->I);
+}
+
 // Which expert kernels can have work, given an upper bound of any expert's
 // slot count (the planner decides on the device; a kernel with an empty
 // list returns at once, but one that cannot have work is not launched).
@@ -270,7 +280,8 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
                        const int32_t* perm, const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
                        const __nv_bfloat16* Wd, __nv_bfloat16* x_sorted,
                        __nv_bfloat16* h, __nv_bfloat16* y, const Plan& plan,
-                       int64_t fat_bound, cudaStream_t s, cudaEvent_t* ev) {
+                       int64_t fat_bound, cudaStream_t s, cudaEvent_t* ev,
+                       const SelfRoute* sr = nullptr) {
     const int64_t P = (int64_t)sh->T * sh->k;
     const ExpertKernels kn = expert_kernels(sh, fat_bound);
     const int64_t ra = rows_alloc(P);
@@ -291,7 +302,8 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
     {
         const Nvtx r("moe.thin_gate_up");
         if (kn.units)
-            CUDA_TRY(launch_thin_gate_up(x, perm, sh->k, H, I, Wg, Wu, plan, fat_bound, h, sms, s),
+            CUDA_TRY(launch_thin_gate_up(x, perm, sh->k, H, I, Wg, Wu, plan, fat_bound, h, sms, s,
+                                         sr),
                      "thin gate/up");
         if (kn.mma)
             CUDA_TRY(launch_thin_mma_gate_up(x_sorted, ra, Wg, Wu, H, I, plan, h, sms, s),
@@ -308,7 +320,7 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
     {
         const Nvtx r("moe.thin_down");
         if (kn.units)
-            CUDA_TRY(launch_thin_down(h, H, I, Wd, plan, fat_bound, y, sms, s), "thin down");
+            CUDA_TRY(launch_thin_down(h, H, I, Wd, plan, fat_bound, y, sms, s, sr), "thin down");
         if (kn.mma)
             CUDA_TRY(launch_thin_mma_down(h, ra, Wd, H, I, plan, y, sms, s),
                      "thin down (tensor cores)");
@@ -454,19 +466,25 @@ static moe_status forward_impl(const moe_shape* shape, const float* logits, cons
     float* g = gates ? gates : b.gates;
     const Nvtx range("moe_forward");
     CUDA_TRY(mark(ev, kEvStart, s), "cudaEventRecord");
-    {
-        const Nvtx r("moe.route");
-        CUDA_TRY(launch_route(logits, T, E, k, idx, g, s), "route");
-    }
-    CUDA_TRY(mark(ev, kEvRoute, s), "cudaEventRecord");
     Plan plan = make_plan(shape, b.tiles, b.solo_tiles, b.units, b.mma_tiles, b.hdr);
     if (wslot) {
         plan.wslot = wslot;
         plan.n_wblocks = n_wblocks;
     }
+    // Small batches route inside the streaming kernels and combine in the down
+    // kernel (the route, permute and combine stages are then empty); the
+    // others run the router, the route lists and the combine kernel.
+    const bool self = self_routed(shape);
+    const SelfRoute sr{logits, T, E, k, idx, g, b.counts, b.offsets, b.perm, b.inv_perm,
+                       b.units, (__nv_bfloat16*)out};
+    if (!self) {
+        const Nvtx r("moe.route");
+        CUDA_TRY(launch_route(logits, T, E, k, idx, g, s), "route");
+    }
+    CUDA_TRY(mark(ev, kEvRoute, s), "cudaEventRecord");
     const int64_t P = (int64_t)T * k;
     const int64_t nch = (P + kPermChunk - 1) / kPermChunk;
-    {
+    if (!self) {
         const Nvtx r("moe.permute");
         CUDA_TRY(launch_permute(idx, T, E, k, b.counts, b.offsets, b.perm, b.inv_perm, b.chunk,
                                 b.chunk + nch * E, b.hdr, &plan, s), "permute");
@@ -477,9 +495,9 @@ static moe_status forward_impl(const moe_shape* shape, const float* logits, cons
     // y_sorted reuses its storage.
     st = run_experts(shape, dev, (const __nv_bfloat16*)x, b.perm, (const __nv_bfloat16*)W_gate,
                      (const __nv_bfloat16*)W_up, (const __nv_bfloat16*)W_down, b.xy, b.h, b.xy,
-                     plan, T, s, ev);
+                     plan, T, s, ev, self ? &sr : nullptr);
     if (st != MOE_OK) return st;
-    {
+    if (!self) {
         const Nvtx r("moe.combine");
         CUDA_TRY(launch_combine(b.xy, b.inv_perm, g, T, k, shape->H, (__nv_bfloat16*)out,
                                 dev.num_sms, s), "combine");
@@ -524,6 +542,7 @@ moe_status moe_forward_profiled(const moe_shape* shape, const float* logits,
 int32_t moe_forward_launches(const moe_shape* shape) {
     if (check_shape(shape) != MOE_OK) return -1;
     if (shape->T == 0) return 0;
+    if (self_routed(shape)) return 2;                // gate/up, down (routing, combine inside)
     const int64_t P = (int64_t)shape->T * shape->k;
     int32_t n = 1;                                   // route
     n += (P <= kPermChunk) ? 1 : 3;                  // route lists (+ planner)

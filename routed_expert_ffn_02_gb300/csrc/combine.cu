@@ -2,8 +2,10 @@
 // dsv41-flash-offload wiki, file map):
 //   out[t] = bf16( sum_{j<k} gates[t,j] * y_sorted[inv_perm[t*k + j]] )
 // fp32 accumulation in ascending j, no atomics, so repeated runs are
-// bit-identical.  One block per token row (grid-stride), 16-byte vectors.
+// bit-identical (combine_dev.cuh).  One block per token row (grid-stride),
+// 16-byte vectors.
 #include "moe_internal.cuh"
+#include "combine_dev.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -16,6 +18,7 @@ combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ inv_perm
     ptx::grid_dep_wait();
     ptx::grid_dep_launch();
     const int vec = H / 8;
+    auto load = [&](int64_t i) { return __ldg(y + i); };
     for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
         int64_t src[kMaxK];
         float g[kMaxK];
@@ -24,29 +27,8 @@ combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ inv_perm
             src[j] = (j < k) ? (int64_t)inv_perm[t * k + j] * vec : 0;
             g[j] = (j < k) ? gates[t * k + j] : 0.f;
         }
-        for (int v = threadIdx.x; v < vec; v += blockDim.x) {
-            float acc[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-#pragma unroll
-            for (int j = 0; j < kMaxK; ++j) {
-                if (j < k) {
-                    const uint4 r = __ldg(y + src[j] + v);
-                    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&r);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float2 f = __bfloat1622float2(p[q]);
-                        acc[2 * q] = fmaf(g[j], f.x, acc[2 * q]);
-                        acc[2 * q + 1] = fmaf(g[j], f.y, acc[2 * q + 1]);
-                    }
-                }
-            }
-            uint4 o;
-            __nv_bfloat162* po = reinterpret_cast<__nv_bfloat162*>(&o);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) po[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-            out[t * vec + v] = o;
-        }
+        for (int v = threadIdx.x; v < vec; v += blockDim.x)
+            out[t * vec + v] = combine_vec(load, src, g, k, v);
     }
 }
 

@@ -29,7 +29,8 @@ struct WsHeader {
     int32_t thin_weight;   // sum of thin_unit_cost over those units
     int32_t n_thin_mma;    // thin experts on the tensor-core streaming kernel
     int32_t n_solo;        // fat experts' leftover 128-row tiles (one-CTA GEMM)
-    int32_t reserved[58];
+    int32_t ticket;        // CTAs of a streaming down kernel done (fused combine)
+    int32_t reserved[57];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -130,6 +131,34 @@ __device__ __forceinline__ int weight_block(const int32_t* wslot, int e) {
     return wslot ? __ldg(wslot + e) : e;
 }
 
+// Small batches route inside the CUDA-core streaming kernels: with at most
+// kSelfRouteSlots token slots, every touched expert thin, on the CUDA-core
+// kernel and in one unit, each CTA of the gate/up kernel computes the top-k,
+// the route lists and the units of the whole batch in shared memory
+// (small_plan.cuh) instead of reading a plan written by the router and
+// route-list kernels, CTA 0 stores them, the down kernel reads them, and the
+// last CTA of the down kernel combines the batch: a decode step is two
+// launches, and the weight stream starts right after the first one's wait.
+// logits == nullptr: the kernels read the Plan instead.
+constexpr int kSelfRouteSlots = 32;
+struct SelfRoute {
+    const float* logits;   // [T, E] fp32
+    int32_t T, E, k;
+    // Written by CTA 0 of the gate/up kernel as the router, route-list and
+    // planner kernels would write them; read back by the down kernel.
+    int32_t* idx;          // [T * k]
+    float* gates;          // [T * k]
+    int32_t* counts;       // [E]
+    int32_t* offsets;      // [E + 1]
+    int32_t* perm;         // [T * k]
+    int32_t* inv_perm;     // [T * k]
+    ThinUnit* units;       // the plan's unit list
+    // Layer output [T, H]: the last CTA of the down kernel to finish combines
+    // the batch (the combine kernel's arithmetic) and no combine is launched.
+    __nv_bfloat16* out;
+};
+
+
 // By default every thin expert streams on the tensor cores once at least this
 // many 128-row gate/up work items can exist (touched experts x I/128), and
 // on CUDA cores below it.  Measured on GB300 (H=4096, I=2048): decode batch 2
@@ -171,14 +200,15 @@ cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* perm, int k,
 
 // max_slots: an upper bound of any expert's slot count (sizes the staged
 // activation buffer; units never hold more than plan.unit_tokens).
+// sr != nullptr: the kernels route the batch themselves (see SelfRoute).
 cudaError_t launch_thin_gate_up(const __nv_bfloat16* x, const int32_t* perm, int k, int H,
                                 int I, const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
                                 const Plan& plan, int64_t max_slots, __nv_bfloat16* h,
-                                int num_sms, cudaStream_t s);
+                                int num_sms, cudaStream_t s, const SelfRoute* sr = nullptr);
 
 cudaError_t launch_thin_down(const __nv_bfloat16* h, int H, int I, const __nv_bfloat16* Wd,
                              const Plan& plan, int64_t max_slots, __nv_bfloat16* y_sorted,
-                             int num_sms, cudaStream_t s);
+                             int num_sms, cudaStream_t s, const SelfRoute* sr = nullptr);
 
 // Weight streaming on tcgen05 for the thin experts in plan.mma_tiles:
 // gate_up: h[rows] = silu(x_sorted[rows] Wg_e^T) * (x_sorted[rows] Wu_e^T);

@@ -1,5 +1,5 @@
 // route_dev.cuh -- the per-token top-k router, shared by the router kernel
-// and the fused small-batch route + route-list kernel.
+// and the streaming kernels that route small batches themselves.
 //
 // Each token is routed to k of the layer's E experts (dsv41-flash-offload
 // wiki, overview).  Selection compares raw fp32 logits under the total order
@@ -31,7 +31,10 @@ __device__ __forceinline__ float order_to_float(uint32_t o) {
 }
 
 // One warp routes one token: writes idx[0, k) (experts in selection order)
-// and gates[0, k).  All 32 lanes call it together.
+// and gates[0, k).  All 32 lanes call it together.  The selection rounds are
+// a loop (lane r keeps the r-th winner), so the routine stays a few hundred
+// instructions long: it runs once per launch inside much larger kernels,
+// where an unrolled copy cost more in instruction fetch than in arithmetic.
 template <int EPL>   // candidates per lane
 __device__ __forceinline__ void route_row(const float* __restrict__ row, int E, int k,
                                           int32_t* __restrict__ idx, float* __restrict__ gates) {
@@ -45,46 +48,39 @@ __device__ __forceinline__ void route_row(const float* __restrict__ row, int E, 
                          : 0ull;
     }
 
-    float sel_val[kMaxK];
-    int sel_idx[kMaxK];
+    float sel_val = 0.f;   // lane r < k: the r-th selected logit and its expert
+    int sel_idx = 0;
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) {
+        uint64_t best = 0ull;
 #pragma unroll
-    for (int r = 0; r < kMaxK; ++r) {
-        sel_val[r] = 0.f;
-        sel_idx[r] = 0;
-        if (r < k) {
-            uint64_t best = 0ull;
+        for (int j = 0; j < EPL; ++j) best = key[j] > best ? key[j] : best;
 #pragma unroll
-            for (int j = 0; j < EPL; ++j) best = key[j] > best ? key[j] : best;
+        for (int off = 16; off > 0; off >>= 1) {
+            const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
+            best = o > best ? o : best;
+        }
+        // The owner retires the winner (keys are unique: indices differ).
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
-                best = o > best ? o : best;
-            }
-            // The owner retires the winner (keys are unique: indices differ).
-#pragma unroll
-            for (int j = 0; j < EPL; ++j)
-                if (key[j] == best) key[j] = 0ull;
-            sel_val[r] = order_to_float((uint32_t)(best >> 32));
-            sel_idx[r] = (int)(~(uint32_t)(best & 0xffffffffull));
+        for (int j = 0; j < EPL; ++j)
+            if (key[j] == best) key[j] = 0ull;
+        if (lane == r) {
+            sel_val = order_to_float((uint32_t)(best >> 32));
+            sel_idx = (int)(~(uint32_t)(best & 0xffffffffull));
         }
     }
 
-    // Softmax over the selection, relative to the largest selected logit.
-    const float m = sel_val[0];
-    float w[kMaxK];
+    // Softmax over the selection, relative to the largest selected logit; the
+    // denominator sums the k weights in selection order.
+    const float m = __shfl_sync(0xffffffffu, sel_val, 0);
+    const float w = (lane < k) ? expf(sel_val - m) : 0.f;
     float denom = 0.f;
-#pragma unroll
-    for (int r = 0; r < kMaxK; ++r) {
-        w[r] = (r < k) ? expf(sel_val[r] - m) : 0.f;
-        denom += w[r];
-    }
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) denom += __shfl_sync(0xffffffffu, w, r);
     // Lane r writes output r (coalesced).
-#pragma unroll
-    for (int r = 0; r < kMaxK; ++r) {
-        if (r < k && lane == r) {
-            idx[r] = sel_idx[r];
-            gates[r] = w[r] / denom;
-        }
+    if (lane < k) {
+        idx[lane] = sel_idx;
+        gates[lane] = w / denom;
     }
 }
 

@@ -1,0 +1,169 @@
+// small_plan.cuh -- routing, route lists and weight-streaming units of a
+// small batch (at most kSelfRouteSlots token slots), computed by every CTA of
+// a streaming kernel in its own shared memory (see SelfRoute).
+//
+// The results are those of the router, route-list and planner kernels for
+// the same batch: the top-k and gates come from the same per-token routine
+// (route_dev.cuh); the route lists are the stable counting sort of the slots
+// s = t*k + j by expert (position of a slot = number of slots with a smaller
+// (expert, s) key, the keys being distinct); each touched expert is one unit
+// of all its slots, in ascending expert order, priced by thin_unit_cost.
+#pragma once
+
+#include "combine_dev.cuh"
+#include "moe_internal.cuh"
+#include "route_dev.cuh"
+
+namespace moe {
+
+struct SmallPlan {
+    int32_t idx[kSelfRouteSlots];       // slot -> expert
+    float gates[kSelfRouteSlots];       // slot -> gate
+    int32_t perm[kSelfRouteSlots];      // sorted position -> slot
+    int32_t inv_perm[kSelfRouteSlots];  // slot -> sorted position
+    ThinUnit units[kSelfRouteSlots];    // one per touched expert
+    int32_t n_units;
+    int32_t weight;                     // sum of thin_unit_cost over the units
+};
+
+// One warp routes one token row (all 32 lanes call it), with the candidates
+// per lane the router kernel uses for E.
+__device__ __noinline__ void route_token(const float* row, int E, int k, int32_t* idx,
+                                         float* gates) {
+    const int epl = (E + 31) / 32;
+    if (epl <= 1) routing::route_row<1>(row, E, k, idx, gates);
+    else if (epl <= 2) routing::route_row<2>(row, E, k, idx, gates);
+    else if (epl <= 4) routing::route_row<4>(row, E, k, idx, gates);
+    else if (epl <= 8) routing::route_row<8>(row, E, k, idx, gates);
+    else if (epl <= 12) routing::route_row<12>(row, E, k, idx, gates);
+    else if (epl <= 16) routing::route_row<16>(row, E, k, idx, gates);
+    else if (epl <= 24) routing::route_row<24>(row, E, k, idx, gates);
+    else routing::route_row<32>(row, E, k, idx, gates);
+}
+
+// Called by every thread of the block.  Warp w routes tokens w, w + warps,
+// ...; then warp 0 (lane = slot, later lane = sorted position) builds the
+// route lists and the units.  Requires T * k <= kSelfRouteSlots and E <= 1024.
+__device__ inline void build_small_plan(const SelfRoute& sr, SmallPlan& sp) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_warps = blockDim.x >> 5;
+    for (int t = warp; t < sr.T; t += n_warps)
+        route_token(sr.logits + (int64_t)t * sr.E, sr.E, sr.k, sp.idx + t * sr.k,
+                    sp.gates + t * sr.k);
+    __syncthreads();
+    if (warp == 0) {
+        const int P = sr.T * sr.k;
+        const bool live = lane < P;
+        // key = expert * 32 + slot: distinct, ordered by (expert, slot)
+        const uint32_t key = live ? ((uint32_t)sp.idx[lane] << 5) | (uint32_t)lane : 0xffffffffu;
+        int pos = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pos += __shfl_sync(0xffffffffu, key, j) < key ? 1 : 0;
+        if (live) {
+            sp.perm[pos] = lane;
+            sp.inv_perm[lane] = pos;
+        }
+        __syncwarp();
+        // lane p: sorted position p; a unit starts where the expert changes
+        const int e = live ? sp.idx[sp.perm[lane]] : -1;
+        const int e_prev = __shfl_up_sync(0xffffffffu, e, 1);
+        const bool head = live && (lane == 0 || e_prev != e);
+        const unsigned heads = __ballot_sync(0xffffffffu, head);
+        const unsigned later = lane < 31 ? heads & ~((2u << lane) - 1u) : 0u;
+        const int n = (later ? __ffs(later) - 1 : P) - lane;
+        const int cost = head ? thin_unit_cost(n) : 0;
+        int incl = cost;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (head) {
+            ThinUnit u;
+            u.expert = e;
+            u.row0 = lane;
+            u.n = n;
+            u.cost_before = incl - cost;
+            sp.units[__popc(heads & ((1u << lane) - 1u))] = u;
+        }
+        if (lane == 31) {
+            sp.n_units = __popc(heads);
+            sp.weight = incl;
+        }
+    }
+    __syncthreads();
+}
+
+// Called by every thread of one block: writes the batch's router outputs,
+// route lists, units and planner counts where the router, route-list and
+// planner kernels would have written them.
+__device__ inline void write_small_plan(const SelfRoute& sr, const SmallPlan& sp, WsHeader* hdr) {
+    const int P = sr.T * sr.k;
+    for (int s = threadIdx.x; s < P; s += blockDim.x) {
+        sr.idx[s] = sp.idx[s];
+        sr.gates[s] = sp.gates[s];
+        sr.perm[s] = sp.perm[s];
+        sr.inv_perm[s] = sp.inv_perm[s];
+    }
+    for (int u = threadIdx.x; u < sp.n_units; u += blockDim.x) sr.units[u] = sp.units[u];
+    for (int e = threadIdx.x; e <= sr.E; e += blockDim.x) {
+        int c = 0, before = 0;
+        for (int s = 0; s < P; ++s) {
+            c += sp.idx[s] == e ? 1 : 0;
+            before += sp.idx[s] < e ? 1 : 0;
+        }
+        if (e < sr.E) sr.counts[e] = c;
+        sr.offsets[e] = before;   // offsets[E] = P
+    }
+    if (threadIdx.x == 0) {
+        hdr->ticket = 0;   // the down kernel's fused combine counts CTAs on it
+        hdr->n_fat_tiles = 0;
+        hdr->n_thin = sp.n_units;
+        hdr->thin_weight = sp.weight;
+        hdr->n_thin_mma = 0;
+        hdr->n_solo = 0;
+    }
+}
+
+// Called by every thread of the block, after the kernel that ran
+// write_small_plan has completed: the batch's units, gates and route lists
+// back into shared memory (only what the streaming down kernel and its fused
+// combine read).  The unit list holds at least min(E, T*k) entries.
+__device__ inline void load_small_plan(const SelfRoute& sr, const WsHeader* hdr, SmallPlan& sp) {
+    const int P = sr.T * sr.k;
+    const int nu = P < sr.E ? P : sr.E;
+    for (int i = threadIdx.x; i < P; i += blockDim.x) {
+        sp.gates[i] = sr.gates[i];
+        sp.inv_perm[i] = sr.inv_perm[i];
+        if (i < nu) sp.units[i] = sr.units[i];
+    }
+    if (threadIdx.x == 0) {
+        sp.n_units = hdr->n_thin;
+        sp.weight = hdr->thin_weight;
+    }
+    __syncthreads();
+}
+
+// Called by every thread of one block: out[t] for every token of the batch,
+// from y_sorted rows written by other CTAs of the same kernel (read through
+// L2) and the batch's gates and route lists in sp.
+__device__ inline void combine_small(const SelfRoute& sr, const SmallPlan& sp,
+                                     const __nv_bfloat16* y_sorted, int H) {
+    const int vec = H / 8;
+    const uint4* y = reinterpret_cast<const uint4*>(y_sorted);
+    uint4* out = reinterpret_cast<uint4*>(sr.out);
+    auto load = [&](int64_t i) { return __ldcg(y + i); };
+    for (int t = 0; t < sr.T; ++t) {
+        int64_t src[kMaxK];
+        float g[kMaxK];
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            src[j] = (j < sr.k) ? (int64_t)sp.inv_perm[t * sr.k + j] * vec : 0;
+            g[j] = (j < sr.k) ? sp.gates[t * sr.k + j] : 0.f;
+        }
+        for (int v = threadIdx.x; v < vec; v += blockDim.x)
+            out[(int64_t)t * vec + v] = combine_vec(load, src, g, sr.k, v);
+    }
+}
+
+}  // namespace moe

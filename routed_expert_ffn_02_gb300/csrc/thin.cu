@@ -45,6 +45,8 @@
 
 #include "moe_internal.cuh"
 #include "ptx.cuh"
+#include "combine_dev.cuh"
+#include "small_plan.cuh"
 
 namespace moe {
 namespace {
@@ -184,17 +186,17 @@ __device__ __forceinline__ int item_at(const ThinUnit* units, int n_units, int i
     return lo * ipe + (int)(k < ipe ? k : ipe);
 }
 
-// This CTA's contiguous share of the items, of (about) equal total cost.
-__device__ __forceinline__ Range cta_range(const ThinUnit* units, const WsHeader* hdr, int ipe) {
+// This CTA's contiguous share of the items of n_units units of total cost
+// `weight` (per item), of (about) equal total cost.
+__device__ __forceinline__ Range cta_range(const ThinUnit* units, int n_units, int weight, int ipe) {
     Range r;
-    const int n_units = hdr->n_thin;
     if (n_units <= 0) {
         r.beg = r.cnt = 0;
         r.u_first = 0;
         r.u_last = -1;
         return r;
     }
-    const int64_t total = (int64_t)hdr->thin_weight * ipe;
+    const int64_t total = (int64_t)weight * ipe;
     const int64_t c0 = total * blockIdx.x / gridDim.x;
     const int64_t c1 = total * (blockIdx.x + 1) / gridDim.x;
     r.beg = item_at(units, n_units, ipe, c0);
@@ -602,17 +604,33 @@ thin_gate_up_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
                     const __nv_bfloat16* __restrict__ Wu, const ThinUnit* __restrict__ units,
                     const int32_t* __restrict__ wslot,
                     WsHeader* hdr, __nv_bfloat16* __restrict__ h, int stage_bytes, int slots,
-                    int act_bytes) {
+                    int act_bytes, SelfRoute sr) {
     extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ SmallPlan sp;
     constexpr int kProducers = 2;   // warp 0 issues the gate rows, warp 1 the up rows
     const int nc = (blockDim.x >> 5) - kProducers;
     const Smem m = smem_setup(smem, stage_bytes, slots, act_bytes, kProducers, nc);
-    grid_dep_wait();      // the plan may come from the previous kernel
+    grid_dep_wait();      // the plan (or the logits) may come from the previous kernel
     grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int vec = H / 8;
     const int ipe = I / R;
-    const Range rg = cta_range(units, hdr, ipe);
+    // The units and the slot order: the plan's, or the batch's own routing.
+    const ThinUnit* U = units;
+    const int32_t* order = perm;
+    int n_units, weight;
+    if (sr.logits) {
+        build_small_plan(sr, sp);
+        if (blockIdx.x == 0) write_small_plan(sr, sp, hdr);
+        U = sp.units;
+        order = sp.perm;
+        n_units = sp.n_units;
+        weight = sp.weight;
+    } else {
+        n_units = hdr->n_thin;
+        weight = hdr->thin_weight;
+    }
+    const Range rg = cta_range(U, n_units, weight, ipe);
     const uint32_t half = (uint32_t)R * H * 2;
     const uint32_t xrow = (uint32_t)H * 2;
 
@@ -624,25 +642,25 @@ thin_gate_up_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
             const bool ok = produce(
                 m, rg, warp == 0,
                 [&](int it, uint32_t dst, uint32_t bar) {
-                    const ThinUnit un = units[it / ipe];
+                    const ThinUnit un = U[it / ipe];
                     const size_t off =
                         ((size_t)weight_block(wslot, un.expert) * I + (size_t)(it % ipe) * R) * H;
                     mbar_expect_tx(bar, half);
                     bulk_g2s_evict_first(dst + part, W + off, half, bar, policy);
                 },
                 [&](int u, uint32_t dst, uint32_t bar) {
-                    const ThinUnit un = units[u];
+                    const ThinUnit un = U[u];
                     mbar_expect_tx(bar, (uint32_t)un.n * xrow);
                     for (int t = 0; t < un.n; ++t)
-                        bulk_g2s(dst + t * xrow, x + (size_t)(perm[un.row0 + t] / k) * H, xrow, bar);
+                        bulk_g2s(dst + t * xrow, x + (size_t)(order[un.row0 + t] / k) * H, xrow, bar);
                 });
             if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
         }
         return;
     }
 
-    const bool ok = consume<16>(m, rg, ipe, units, warp - kProducers, nc, [&]<int N>(int it, int slot) {
-        const ThinUnit un = units[it / ipe];
+    const bool ok = consume<16>(m, rg, ipe, U, warp - kProducers, nc, [&]<int N>(int it, int slot) {
+        const ThinUnit un = U[it / ipe];
         __nv_bfloat16* hcol = h + (int64_t)un.row0 * I + (it % ipe) * R;
         gate_up_slot<N, VPL>(m, slot, R, vec, un.n, hcol, I);
     });
@@ -656,8 +674,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 thin_down_kernel(const __nv_bfloat16* __restrict__ h, int H, int I, int R,
                  const __nv_bfloat16* __restrict__ Wd, const ThinUnit* __restrict__ units,
                  const int32_t* __restrict__ wslot, WsHeader* hdr,
-                 __nv_bfloat16* __restrict__ y, int stage_bytes, int slots, int act_bytes) {
+                 __nv_bfloat16* __restrict__ y, int stage_bytes, int slots, int act_bytes,
+                 SelfRoute sr) {
     extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ SmallPlan sp;
     constexpr int kProducers = 1;
     const int nc = (blockDim.x >> 5) - kProducers;
     const Smem m = smem_setup(smem, stage_bytes, slots, act_bytes, kProducers, nc);
@@ -668,8 +688,22 @@ thin_down_kernel(const __nv_bfloat16* __restrict__ h, int H, int I, int R,
     // previous kernel on the stream (at least the gate/up kernel runs in
     // between) and so have completed when this kernel starts; W_down is read
     // only.  So the CTA's range and its first round of weight rows are
-    // fetched before waiting for the previous kernel; h and y after.
-    const Range rg = cta_range(units, hdr, ipe);
+    // fetched before waiting for the previous kernel; h and y after.  A batch
+    // that routes itself has its plan written by the gate/up kernel, the
+    // previous launch: it is read after the wait.
+    const ThinUnit* U = units;
+    int n_units, weight;
+    if (sr.logits) {
+        grid_dep_wait();
+        load_small_plan(sr, hdr, sp);
+        U = sp.units;
+        n_units = sp.n_units;
+        weight = sp.weight;
+    } else {
+        n_units = hdr->n_thin;
+        weight = hdr->thin_weight;
+    }
+    const Range rg = cta_range(U, n_units, weight, ipe);
     const uint32_t bytes = (uint32_t)R * I * 2;
     const uint32_t hrow = (uint32_t)I * 2;
 
@@ -677,7 +711,7 @@ thin_down_kernel(const __nv_bfloat16* __restrict__ h, int H, int I, int R,
         if (lane == 0) {
             const uint64_t policy = policy_evict_first();
             auto copy_item = [&](int it, uint32_t dst, uint32_t bar) {
-                const ThinUnit un = units[it / ipe];
+                const ThinUnit un = U[it / ipe];
                 mbar_expect_tx(bar, bytes);
                 bulk_g2s_evict_first(
                     dst, Wd + ((size_t)weight_block(wslot, un.expert) * H + (size_t)(it % ipe) * R) * I,
@@ -690,7 +724,7 @@ thin_down_kernel(const __nv_bfloat16* __restrict__ h, int H, int I, int R,
             const bool ok = produce(
                 m, rg, true, copy_item,
                 [&](int u, uint32_t dst, uint32_t bar) {
-                    const ThinUnit un = units[u];
+                    const ThinUnit un = U[u];
                     // the unit's h rows are consecutive sorted positions
                     mbar_expect_tx(bar, (uint32_t)un.n * hrow);
                     bulk_g2s(dst, h + (size_t)un.row0 * I, (uint32_t)un.n * hrow, bar);
@@ -698,18 +732,34 @@ thin_down_kernel(const __nv_bfloat16* __restrict__ h, int H, int I, int R,
                 pre);
             if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
         }
-        return;
+    } else {
+        grid_dep_wait();      // consumers write y
+        grid_dep_launch();
+        constexpr int kExact =
+            (VPL > 0 && DownRegSlots<VPL>::value > 0) ? DownRegSlots<VPL>::value : 16;
+        const bool ok = consume<kExact>(m, rg, ipe, U, warp - kProducers, nc,
+                                        [&]<int N>(int it, int slot) {
+            const ThinUnit un = U[it / ipe];
+            __nv_bfloat16* ycol = y + (int64_t)un.row0 * H + (it % ipe) * R;
+            down_slot<N, VPL>(m, slot, R, vec, un.n, ycol, H);
+        });
+        if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
     }
-    grid_dep_wait();      // consumers write y
-    grid_dep_launch();
-
-    constexpr int kExact = (VPL > 0 && DownRegSlots<VPL>::value > 0) ? DownRegSlots<VPL>::value : 16;
-    const bool ok = consume<kExact>(m, rg, ipe, units, warp - kProducers, nc, [&]<int N>(int it, int slot) {
-        const ThinUnit un = units[it / ipe];
-        __nv_bfloat16* ycol = y + (int64_t)un.row0 * H + (it % ipe) * R;
-        down_slot<N, VPL>(m, slot, R, vec, un.n, ycol, H);
-    });
-    if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
+    if (sr.out) {
+        // Fused combine: every thread fences its y stores, then the CTA takes
+        // a ticket; the CTA that takes the last one has every CTA's rows in
+        // view and combines the batch.  The gate/up kernel zeroed the ticket.
+        __shared__ int s_last;
+        grid_dep_wait();
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) s_last = atomicAdd(&hdr->ticket, 1) == (int)gridDim.x - 1;
+        __syncthreads();
+        if (s_last) {
+            __threadfence();
+            combine_small(sr, sp, y, H);
+        }
+    }
 }
 
 // Rows per item so that a weight slot holds at most kStageTarget bytes (at
@@ -751,24 +801,26 @@ int threads_for(const Geometry& g, int producers) {
 template <int V>
 cudaError_t launch_gu(const __nv_bfloat16* x, const int32_t* perm, int k, int H, int I,
                       const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, const Plan& plan,
-                      const Geometry& g, __nv_bfloat16* h, int num_sms, cudaStream_t s) {
+                      const Geometry& g, __nv_bfloat16* h, int num_sms, cudaStream_t s,
+                      const SelfRoute& sr) {
     static std::atomic<int> done[kMaxDevices];
     cudaError_t e = smem_limit_once(thin_gate_up_kernel<V>, kSmemBudget + 1024, done);
     if (e != cudaSuccess) return e;
     return launch_pdl(thin_gate_up_kernel<V>, dim3(num_sms), dim3(threads_for(g, 2)), g.smem, s,
                       x, perm, k, H, I, g.R, Wg, Wu, plan.units, plan.wslot, plan.hdr, h, g.stage,
-                      g.slots, g.act);
+                      g.slots, g.act, sr);
 }
 
 template <int V>
 cudaError_t launch_d(const __nv_bfloat16* h, int H, int I, const __nv_bfloat16* Wd,
                      const Plan& plan, const Geometry& g, __nv_bfloat16* y, int num_sms,
-                     cudaStream_t s) {
+                     cudaStream_t s, const SelfRoute& sr) {
     static std::atomic<int> done[kMaxDevices];
     cudaError_t e = smem_limit_once(thin_down_kernel<V>, kSmemBudget + 1024, done);
     if (e != cudaSuccess) return e;
     return launch_pdl(thin_down_kernel<V>, dim3(num_sms), dim3(threads_for(g, 1)), g.smem, s, h,
-                      H, I, g.R, Wd, plan.units, plan.wslot, plan.hdr, y, g.stage, g.slots, g.act);
+                      H, I, g.R, Wd, plan.units, plan.wslot, plan.hdr, y, g.stage, g.slots, g.act,
+                      sr);
 }
 
 }  // namespace
@@ -783,7 +835,8 @@ int thin_unit_tokens(int H, int I) {
 cudaError_t launch_thin_gate_up(const __nv_bfloat16* x, const int32_t* perm, int k, int H,
                                 int I, const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
                                 const Plan& plan, int64_t max_slots, __nv_bfloat16* h,
-                                int num_sms, cudaStream_t s) {
+                                int num_sms, cudaStream_t s, const SelfRoute* sr) {
+    const SelfRoute self = sr ? *sr : SelfRoute{};
     const int act_tokens =
         (int)std::min<int64_t>(plan.unit_tokens, std::max<int64_t>(max_slots, 1));
     const Geometry g = geometry(2 * H * 2, H * 2, act_tokens, false);
@@ -792,18 +845,19 @@ cudaError_t launch_thin_gate_up(const __nv_bfloat16* x, const int32_t* perm, int
         return cudaErrorInvalidConfiguration;
     }
     switch (g.stage == kStageTarget ? H : 0) {
-        case 256: return launch_gu<1>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s);
-        case 512: return launch_gu<2>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s);
-        case 1024: return launch_gu<4>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s);
-        case 2048: return launch_gu<8>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s);
-        case 4096: return launch_gu<16>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s);
-        default: return launch_gu<0>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s);
+        case 256: return launch_gu<1>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s, self);
+        case 512: return launch_gu<2>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s, self);
+        case 1024: return launch_gu<4>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s, self);
+        case 2048: return launch_gu<8>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s, self);
+        case 4096: return launch_gu<16>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s, self);
+        default: return launch_gu<0>(x, perm, k, H, I, Wg, Wu, plan, g, h, num_sms, s, self);
     }
 }
 
 cudaError_t launch_thin_down(const __nv_bfloat16* h, int H, int I, const __nv_bfloat16* Wd,
                              const Plan& plan, int64_t max_slots, __nv_bfloat16* y_sorted,
-                             int num_sms, cudaStream_t s) {
+                             int num_sms, cudaStream_t s, const SelfRoute* sr) {
+    const SelfRoute self = sr ? *sr : SelfRoute{};
     const int act_tokens =
         (int)std::min<int64_t>(plan.unit_tokens, std::max<int64_t>(max_slots, 1));
     const Geometry g = geometry(I * 2, I * 2, act_tokens, true);
@@ -812,13 +866,13 @@ cudaError_t launch_thin_down(const __nv_bfloat16* h, int H, int I, const __nv_bf
         return cudaErrorInvalidConfiguration;
     }
     switch (g.stage == kStageTarget ? I : 0) {
-        case 256: return launch_d<1>(h, H, I, Wd, plan, g, y_sorted, num_sms, s);
-        case 512: return launch_d<2>(h, H, I, Wd, plan, g, y_sorted, num_sms, s);
-        case 1024: return launch_d<4>(h, H, I, Wd, plan, g, y_sorted, num_sms, s);
-        case 2048: return launch_d<8>(h, H, I, Wd, plan, g, y_sorted, num_sms, s);
-        case 4096: return launch_d<16>(h, H, I, Wd, plan, g, y_sorted, num_sms, s);
-        case 8192: return launch_d<32>(h, H, I, Wd, plan, g, y_sorted, num_sms, s);
-        default: return launch_d<0>(h, H, I, Wd, plan, g, y_sorted, num_sms, s);
+        case 256: return launch_d<1>(h, H, I, Wd, plan, g, y_sorted, num_sms, s, self);
+        case 512: return launch_d<2>(h, H, I, Wd, plan, g, y_sorted, num_sms, s, self);
+        case 1024: return launch_d<4>(h, H, I, Wd, plan, g, y_sorted, num_sms, s, self);
+        case 2048: return launch_d<8>(h, H, I, Wd, plan, g, y_sorted, num_sms, s, self);
+        case 4096: return launch_d<16>(h, H, I, Wd, plan, g, y_sorted, num_sms, s, self);
+        case 8192: return launch_d<32>(h, H, I, Wd, plan, g, y_sorted, num_sms, s, self);
+        default: return launch_d<0>(h, H, I, Wd, plan, g, y_sorted, num_sms, s, self);
     }
 }
 

@@ -136,14 +136,23 @@ def test_stager_argument_errors(moe):
 
 def test_forward_launch_count(moe):
     """Kernels one moe_forward launches: route, route lists (1 or 3), then
-    only the expert kernels that can have work, then combine."""
+    only the expert kernels that can have work, then combine.  Small batches
+    on the CUDA-core streaming kernels route inside them and combine in the
+    down kernel: gate/up, down."""
     S = moe.Shape
-    # decode: 8 or 16 touched experts x 16 blocks < 384 items -> CUDA cores
-    assert moe.forward_launches(S(1, 384, 8, 4096, 2048)) == 5
-    assert moe.forward_launches(S(2, 384, 8, 4096, 2048)) == 5
+    # decode: 8 or 16 touched experts x 16 blocks < 384 items -> CUDA cores,
+    # batch routed inside the streaming kernels
+    assert moe.forward_launches(S(1, 384, 8, 4096, 2048)) == 2
+    assert moe.forward_launches(S(2, 384, 8, 4096, 2048)) == 2
     assert moe.forward_launches(S(3, 384, 8, 4096, 2048)) == 6       # 24 x 16 = 384: tensor cores
     assert moe.forward_launches(S(1, 384, 8, 4096, 2048, thin_mma_min=1)) == 6
-    assert moe.forward_launches(S(4, 384, 8, 4096, 2048, thin_mma_min=33)) == 5
+    assert moe.forward_launches(S(4, 384, 8, 4096, 2048, thin_mma_min=33)) == 2
+    # self-routing limits: 32 slots, below the fat threshold, one unit per expert
+    assert moe.forward_launches(S(5, 384, 8, 4096, 2048, thin_mma_min=33)) == 5   # 40 slots
+    assert moe.forward_launches(S(32, 64, 1, 512, 256, thin_mma_min=33)) == 10    # T = 32 may be fat
+    assert moe.forward_launches(S(16, 64, 2, 512, 256, thin_mma_min=33)) == 2     # unit of 16
+    assert moe.forward_launches(S(13, 64, 2, 4096, 2048, thin_mma_min=33)) == 5   # units of 12
+    assert moe.forward_launches(S(2, 64, 2, 512, 256, fat_threshold=0)) == 8     # every expert fat
     # fat experts: pair GEMMs and solo-tile GEMMs for gate/up and down
     assert moe.forward_launches(S(16384, 384, 8, 4096, 2048)) == 12
     assert moe.forward_launches(S(16384, 384, 8, 4096, 2048, thin_mma_min=8)) == 14

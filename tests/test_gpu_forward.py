@@ -143,6 +143,74 @@ def test_forward_threshold_edges(moe, mma_min):
     _full_check(moe, s2, 32, inp, mma_min=mma_min)
 
 
+# Small batches on the CUDA-core streaming kernels route themselves inside
+# them and combine in the down kernel (two launches): T*k <= 32, T below the
+# fat threshold and within one streaming unit.
+SELF_ROUTED = [
+    # T, E, k, H, I
+    (1, 16, 2, 512, 256),
+    (3, 16, 2, 512, 256),
+    (16, 64, 2, 512, 256),     # 32 slots in units of 16
+    (4, 1024, 8, 256, 256),    # E = 1024: 32 router candidates per lane
+    (5, 3, 2, 768, 512),       # sizes that are not powers of two
+    (2, 1, 1, 256, 256),       # a single expert
+    (6, 8, 5, 1280, 768),      # 30 slots, k = 5
+]
+
+
+@pytest.mark.parametrize("T,E,k,H,I", SELF_ROUTED)
+def test_forward_self_routed(moe, T, E, k, H, I):
+    """Routing bit-exact and outputs against the oracle; and bit-identical to
+    the same batch through the separate entry points (router, route lists,
+    expert FFN on the planner's units, combine)."""
+    s = synth.Shape(T=T, E=E, k=k, H=H, I=I)
+    inp = synth.make_layer(s, seed=100 + T, zipf_s=synth.ZIPF_S)
+    d = _to_dev(inp)
+    shape = moe.Shape(T, E, k, H, I, fat_threshold=32, thin_mma_min=MMA_NONE)
+    assert moe.forward_launches(shape) == 2
+    _full_check(moe, s, 32, inp, d, mma_min=MMA_NONE)
+    out, idx, gates = _forward(moe, shape, d)
+    idx2, gates2 = moe.moe_route(d["logits"], k)
+    counts, offsets, perm, inv = moe.moe_permute(idx2, E)
+    y = moe.moe_expert_ffn(shape, d["x"], perm, offsets, counts, d["Wg"], d["Wu"], d["Wd"])
+    out2 = moe.moe_combine(y, inv, gates2, T, k, H)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx2) and torch.equal(gates, gates2)
+    assert torch.equal(out, out2)
+
+
+def test_forward_self_routed_ties_and_reuse(moe):
+    """All-equal logits (every token takes experts 0..k-1, gates 1/k: the
+    lowest-index tie-break), on a workspace that a routed-and-planned prefill
+    batch used before, and that batch again afterwards."""
+    s = synth.Shape(T=4, E=16, k=4, H=512, I=256)
+    inp = synth.make_layer(s, seed=5)
+    inp["logits"] = torch.zeros((s.T, s.E))
+    d = _to_dev(inp)
+    big = synth.Shape(T=64, E=16, k=4, H=512, I=256)
+    binp = synth.make_layer(big, seed=5, zipf_s=synth.ZIPF_S)
+    bd = dict(_to_dev(binp), Wg=d["Wg"], Wu=d["Wu"], Wd=d["Wd"])
+    bshape = moe.Shape(big.T, big.E, big.k, big.H, big.I, fat_threshold=32,
+                       thin_mma_min=MMA_NONE)
+    shape = moe.Shape(s.T, s.E, s.k, s.H, s.I, fat_threshold=32, thin_mma_min=MMA_NONE)
+    ws = moe.Workspace(max(moe.workspace_size(bshape), moe.workspace_size(shape)))
+    first = moe.moe_forward(bshape, bd["logits"], bd["x"], bd["Wg"], bd["Wu"], bd["Wd"], ws=ws)
+    idx = torch.empty((s.T, s.k), dtype=torch.int32, device="cuda")
+    gates = torch.empty((s.T, s.k), dtype=torch.float32, device="cuda")
+    out = moe.moe_forward(shape, d["logits"], d["x"], d["Wg"], d["Wu"], d["Wd"],
+                          topk_idx=idx, gates=gates, ws=ws)
+    again = moe.moe_forward(bshape, bd["logits"], bd["x"], bd["Wg"], bd["Wu"], bd["Wd"], ws=ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    assert torch.equal(first, again)
+    assert np.array_equal(idx.cpu().numpy(), np.tile(np.arange(s.k, dtype=np.int32), (s.T, 1)))
+    assert np.allclose(gates.cpu().numpy(), 1.0 / s.k, rtol=0, atol=GATE_ATOL)
+    experts = DeviceExperts(d["Wg"], d["Wu"], d["Wd"])
+    ref, _, _ = oracle_rows(synth.bf16_bits(inp["x"]), inp["logits"].numpy(), s.k, experts,
+                            np.arange(s.T))
+    assert_close(out, ref, "self-routed ties")
+
+
 def test_forward_gemm_pair_boundaries(moe):
     """The grouped GEMM runs an expert's 128-row tiles in pairs (256 rows per
     CTA pair): slot counts on either side of pair and tile boundaries, so
