@@ -10,9 +10,12 @@
 //   key = order(value) << 32 | ~index
 // where order() maps fp32 to an unsigned integer with the same ordering
 // (-0.0 folded onto +0.0, since they compare equal).  The largest key is the
-// next expert to select; k rounds of a warp max-reduction pick the top k in
-// output order.  Key 0 marks an empty or already-taken candidate and sorts
-// below every real logit, including -inf.
+// next expert to select: each round takes every lane's largest key (a
+// pairwise tree), the warp maximum of their high halves, then the maximum low
+// half among the lanes that hold that high half (two redux.sync warp
+// reductions), and the owner retires it; k rounds give the top k in output
+// order.  Key 0 marks an empty or already-taken candidate and sorts below
+// every real logit, including -inf.
 #pragma once
 
 #include "moe_internal.cuh"
@@ -34,7 +37,9 @@ __device__ __forceinline__ float order_to_float(uint32_t o) {
 // and gates[0, k).  All 32 lanes call it together.  The selection rounds are
 // a loop (lane r keeps the r-th winner), so the routine stays a few hundred
 // instructions long: it runs once per launch inside much larger kernels,
-// where an unrolled copy cost more in instruction fetch than in arithmetic.
+// where an unrolled copy cost more in instruction fetch than in arithmetic;
+// and each round is two warp reductions deep rather than a five-step
+// shuffle tree of 64-bit keys.
 template <int EPL>   // candidates per lane
 __device__ __forceinline__ void route_row(const float* __restrict__ row, int E, int k,
                                           int32_t* __restrict__ idx, float* __restrict__ gates) {
@@ -52,21 +57,24 @@ __device__ __forceinline__ void route_row(const float* __restrict__ row, int E, 
     int sel_idx = 0;
 #pragma unroll 1
     for (int r = 0; r < k; ++r) {
-        uint64_t best = 0ull;
+        uint64_t t[EPL];
 #pragma unroll
-        for (int j = 0; j < EPL; ++j) best = key[j] > best ? key[j] : best;
+        for (int j = 0; j < EPL; ++j) t[j] = key[j];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
-            best = o > best ? o : best;
-        }
+        for (int span = 1; span < EPL; span *= 2)
+#pragma unroll
+            for (int j = 0; j + span < EPL; j += 2 * span) t[j] = t[j + span] > t[j] ? t[j + span] : t[j];
+        const uint32_t hi = (uint32_t)(t[0] >> 32), lo = (uint32_t)t[0];
+        const uint32_t best_hi = __reduce_max_sync(0xffffffffu, hi);
+        const uint32_t best_lo = __reduce_max_sync(0xffffffffu, hi == best_hi ? lo : 0u);
+        const uint64_t best = ((uint64_t)best_hi << 32) | best_lo;
         // The owner retires the winner (keys are unique: indices differ).
 #pragma unroll
         for (int j = 0; j < EPL; ++j)
             if (key[j] == best) key[j] = 0ull;
         if (lane == r) {
-            sel_val = order_to_float((uint32_t)(best >> 32));
-            sel_idx = (int)(~(uint32_t)(best & 0xffffffffull));
+            sel_val = order_to_float(best_hi);
+            sel_idx = (int)(~best_lo);
         }
     }
 
