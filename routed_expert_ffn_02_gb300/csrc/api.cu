@@ -125,14 +125,18 @@ int thin_mma_min(const moe_shape* sh) {
     return touched * (sh->I / 128) >= kThinMmaAutoItems ? 1 : kThinMaxTokens + 1;
 }
 
-// Small batches whose touched experts are all thin, on the CUDA-core streaming
-// kernel and in one unit each are routed inside the streaming kernels and
-// combined by the down kernel (see SelfRoute): no router, route-list, planner
-// or combine launch.  A token's k experts are distinct, so no expert holds
-// more than T slots.
-bool self_routed(const moe_shape* sh) {
-    return (int64_t)sh->T * sh->k <= kSelfRouteSlots && sh->T < sh->fat_threshold &&
-           sh->T < thin_mma_min(sh) && sh->T <= thin_unit_tokens(sh->H, sh->I);
+// Small batches whose touched experts are all thin and on one streaming
+// kernel (CUDA cores with one unit per expert, or tensor cores) are routed
+// inside the streaming kernels and combined by the down kernel (see
+// SelfRoute): no router, route-list, planner, gather or combine launch.  A
+// token's k experts are distinct, so no expert holds more than T slots.
+enum SelfMode { kPlanned = 0, kSelfUnits, kSelfMma };
+SelfMode self_mode(const moe_shape* sh) {
+    if ((int64_t)sh->T * sh->k > kSelfRouteSlots || sh->T >= sh->fat_threshold) return kPlanned;
+    const int mm = thin_mma_min(sh);
+    if (mm <= 1) return kSelfMma;
+    if (sh->T < mm && sh->T <= thin_unit_tokens(sh->H, sh->I)) return kSelfUnits;
+    return kPlanned;
 }
 
 // Which expert kernels can have work, given an upper bound of any expert's
@@ -286,7 +290,7 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
     const ExpertKernels kn = expert_kernels(sh, fat_bound);
     const int64_t ra = rows_alloc(P);
     const int H = sh->H, I = sh->I, sms = dev.num_sms;
-    if (kn.gather()) {
+    if (kn.gather() && !sr) {   // a self-routed batch loads its x rows itself
         const Nvtx r("moe.gather");
         CUDA_TRY(launch_gather(x, perm, sh->k, H, plan, x_sorted, sms, s), "gather");
     }
@@ -306,7 +310,7 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
                                          sr),
                      "thin gate/up");
         if (kn.mma)
-            CUDA_TRY(launch_thin_mma_gate_up(x_sorted, ra, Wg, Wu, H, I, plan, h, sms, s),
+            CUDA_TRY(launch_thin_mma_gate_up(x_sorted, ra, Wg, Wu, H, I, plan, h, sms, s, sr, x),
                      "thin gate/up (tensor cores)");
     }
     CUDA_TRY(mark(ev, kEvThinGateUp, s), "cudaEventRecord");
@@ -322,7 +326,7 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
         if (kn.units)
             CUDA_TRY(launch_thin_down(h, H, I, Wd, plan, fat_bound, y, sms, s, sr), "thin down");
         if (kn.mma)
-            CUDA_TRY(launch_thin_mma_down(h, ra, Wd, H, I, plan, y, sms, s),
+            CUDA_TRY(launch_thin_mma_down(h, ra, Wd, H, I, plan, y, sms, s, sr),
                      "thin down (tensor cores)");
     }
     CUDA_TRY(mark(ev, kEvThinDown, s), "cudaEventRecord");
@@ -474,7 +478,7 @@ static moe_status forward_impl(const moe_shape* shape, const float* logits, cons
     // Small batches route inside the streaming kernels and combine in the down
     // kernel (the route, permute and combine stages are then empty); the
     // others run the router, the route lists and the combine kernel.
-    const bool self = self_routed(shape);
+    const bool self = self_mode(shape) != kPlanned;
     const SelfRoute sr{logits, T, E, k, idx, g, b.counts, b.offsets, b.perm, b.inv_perm,
                        b.units, (__nv_bfloat16*)out};
     if (!self) {
@@ -542,7 +546,7 @@ moe_status moe_forward_profiled(const moe_shape* shape, const float* logits,
 int32_t moe_forward_launches(const moe_shape* shape) {
     if (check_shape(shape) != MOE_OK) return -1;
     if (shape->T == 0) return 0;
-    if (self_routed(shape)) return 2;                // gate/up, down (routing, combine inside)
+    if (self_mode(shape) != kPlanned) return 2;      // gate/up, down (routing, combine inside)
     const int64_t P = (int64_t)shape->T * shape->k;
     int32_t n = 1;                                   // route
     n += (P <= kPermChunk) ? 1 : 3;                  // route lists (+ planner)

@@ -131,9 +131,10 @@ __device__ __forceinline__ int weight_block(const int32_t* wslot, int e) {
     return wslot ? __ldg(wslot + e) : e;
 }
 
-// Small batches route inside the CUDA-core streaming kernels: with at most
-// kSelfRouteSlots token slots, every touched expert thin, on the CUDA-core
-// kernel and in one unit, each CTA of the gate/up kernel computes the top-k,
+// Small batches route inside the streaming kernels: with at most
+// kSelfRouteSlots token slots, every touched expert thin and on one streaming
+// kernel (CUDA cores, each expert in one unit; or tensor cores, each expert
+// one tile), each CTA of the gate/up kernel computes the top-k,
 // the route lists and the units of the whole batch in shared memory
 // (small_plan.cuh) instead of reading a plan written by the router and
 // route-list kernels, CTA 0 stores them, the down kernel reads them, and the
@@ -213,13 +214,17 @@ cudaError_t launch_thin_down(const __nv_bfloat16* h, int H, int I, const __nv_bf
 // Weight streaming on tcgen05 for the thin experts in plan.mma_tiles:
 // gate_up: h[rows] = silu(x_sorted[rows] Wg_e^T) * (x_sorted[rows] Wu_e^T);
 // down: y[rows] = h[rows] Wd_e^T.  x_sorted / h hold rows_alloc rows.
+// sr != nullptr: the batch routes itself (see SelfRoute); the gate/up kernel
+// then reads the tokens' rows of x [sr->T, H] directly (x_sorted unused).
 cudaError_t launch_thin_mma_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_alloc,
                                     const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int H,
                                     int I, const Plan& plan, __nv_bfloat16* h, int num_sms,
-                                    cudaStream_t s);
+                                    cudaStream_t s, const SelfRoute* sr = nullptr,
+                                    const __nv_bfloat16* x = nullptr);
 cudaError_t launch_thin_mma_down(const __nv_bfloat16* h, int64_t rows_alloc,
                                  const __nv_bfloat16* Wd, int H, int I, const Plan& plan,
-                                 __nv_bfloat16* y_sorted, int num_sms, cudaStream_t s);
+                                 __nv_bfloat16* y_sorted, int num_sms, cudaStream_t s,
+                                 const SelfRoute* sr = nullptr);
 
 // One-CTA grouped GEMMs (tcgen05 cta_group::1, 128 x 256 tiles) over
 // plan.solo_tiles, the same products as the pair GEMMs below.

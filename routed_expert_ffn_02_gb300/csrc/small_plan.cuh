@@ -28,8 +28,8 @@ struct SmallPlan {
 
 // One warp routes one token row (all 32 lanes call it), with the candidates
 // per lane the router kernel uses for E.
-__device__ __noinline__ void route_token(const float* row, int E, int k, int32_t* idx,
-                                         float* gates) {
+static __device__ __noinline__ void route_token(const float* row, int E, int k, int32_t* idx,
+                                                float* gates) {
     const int epl = (E + 31) / 32;
     if (epl <= 1) routing::route_row<1>(row, E, k, idx, gates);
     else if (epl <= 2) routing::route_row<2>(row, E, k, idx, gates);
@@ -96,8 +96,10 @@ __device__ inline void build_small_plan(const SelfRoute& sr, SmallPlan& sp) {
 
 // Called by every thread of one block: writes the batch's router outputs,
 // route lists, units and planner counts where the router, route-list and
-// planner kernels would have written them.
-__device__ inline void write_small_plan(const SelfRoute& sr, const SmallPlan& sp, WsHeader* hdr) {
+// planner kernels would have written them (on_mma: the units are the
+// tensor-core streaming kernel's tiles, one per expert with all its slots).
+__device__ inline void write_small_plan(const SelfRoute& sr, const SmallPlan& sp, WsHeader* hdr,
+                                        bool on_mma = false) {
     const int P = sr.T * sr.k;
     for (int s = threadIdx.x; s < P; s += blockDim.x) {
         sr.idx[s] = sp.idx[s];
@@ -118,9 +120,9 @@ __device__ inline void write_small_plan(const SelfRoute& sr, const SmallPlan& sp
     if (threadIdx.x == 0) {
         hdr->ticket = 0;   // the down kernel's fused combine counts CTAs on it
         hdr->n_fat_tiles = 0;
-        hdr->n_thin = sp.n_units;
-        hdr->thin_weight = sp.weight;
-        hdr->n_thin_mma = 0;
+        hdr->n_thin = on_mma ? 0 : sp.n_units;
+        hdr->thin_weight = on_mma ? 0 : sp.weight;
+        hdr->n_thin_mma = on_mma ? sp.n_units : 0;
         hdr->n_solo = 0;
     }
 }
@@ -138,11 +140,20 @@ __device__ inline void load_small_plan(const SelfRoute& sr, const WsHeader* hdr,
         if (i < nu) sp.units[i] = sr.units[i];
     }
     if (threadIdx.x == 0) {
-        sp.n_units = hdr->n_thin;
+        sp.n_units = hdr->n_thin > 0 ? hdr->n_thin : hdr->n_thin_mma;
         sp.weight = hdr->thin_weight;
     }
     __syncthreads();
 }
+
+// The last CTA of a streaming down kernel to finish combines the batch.
+// Called by every thread of the block once its y rows are stored: each
+// thread fences its stores, the CTA takes a ticket from the workspace header
+// (zeroed by the gate/up kernel), and the CTA with the last ticket reads
+// every CTA's rows (through L2) and writes out.  No thread waits on another
+// CTA.
+__device__ inline void combine_if_last(const SelfRoute& sr, const SmallPlan& sp, WsHeader* hdr,
+                                       const __nv_bfloat16* y_sorted, int H);
 
 // Called by every thread of one block: out[t] for every token of the batch,
 // from y_sorted rows written by other CTAs of the same kernel (read through
@@ -163,6 +174,19 @@ __device__ inline void combine_small(const SelfRoute& sr, const SmallPlan& sp,
         }
         for (int v = threadIdx.x; v < vec; v += blockDim.x)
             out[(int64_t)t * vec + v] = combine_vec(load, src, g, sr.k, v);
+    }
+}
+
+__device__ inline void combine_if_last(const SelfRoute& sr, const SmallPlan& sp, WsHeader* hdr,
+                                       const __nv_bfloat16* y_sorted, int H) {
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&hdr->ticket, 1) == (int)gridDim.x - 1;
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        combine_small(sr, sp, y_sorted, H);
     }
 }
 

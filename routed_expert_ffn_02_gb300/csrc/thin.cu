@@ -745,20 +745,9 @@ thin_down_kernel(const __nv_bfloat16* __restrict__ h, int H, int I, int R,
         });
         if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
     }
-    if (sr.out) {
-        // Fused combine: every thread fences its y stores, then the CTA takes
-        // a ticket; the CTA that takes the last one has every CTA's rows in
-        // view and combines the batch.  The gate/up kernel zeroed the ticket.
-        __shared__ int s_last;
+    if (sr.out) {   // fused combine; every thread has waited for the gate/up kernel
         grid_dep_wait();
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) s_last = atomicAdd(&hdr->ticket, 1) == (int)gridDim.x - 1;
-        __syncthreads();
-        if (s_last) {
-            __threadfence();
-            combine_small(sr, sp, y, H);
-        }
+        combine_if_last(sr, sp, hdr, y, H);
     }
 }
 

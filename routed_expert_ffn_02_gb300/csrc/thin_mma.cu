@@ -21,6 +21,13 @@
 // rows (or TMA's zero fill past the tensor); each output column depends only
 // on its own slot row, so they are computed and discarded.
 //
+// Small batches routed inside the kernels (SelfRoute, small_plan.cuh): every
+// gate/up CTA builds the batch's plan in shared memory, one tile per touched
+// expert, and loads each tile's activation rows straight from x with one-row
+// TMA boxes (the 128-byte swizzle follows the shared-memory address, so a row
+// lands where a 32-row box would put it), so no gather runs; the down kernel
+// reads the plan back and its last CTA combines the batch.
+//
 // Persistent, one CTA per SM, warp-specialised like the grouped GEMM:
 // warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM allocator, warps 4-7
 // epilogue; two TMEM accumulator buffers so an item's epilogue overlaps the
@@ -30,6 +37,7 @@
 
 #include "moe_internal.cuh"
 #include "ptx.cuh"
+#include "small_plan.cuh"
 #include "tcgen05.cuh"
 
 namespace moe {
@@ -65,15 +73,18 @@ struct ThinMmaArgs {
     int w_rows_per_expert;    // rows of the weight tensor per expert
     __nv_bfloat16* out;       // [rows_alloc, ld_out]
     int64_t ld_out;
+    SelfRoute sr;             // logits != nullptr: the batch routes itself
 };
 
 template <bool kGated>
 __global__ void __launch_bounds__(256, 1)
 thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
                 const __grid_constant__ CUtensorMap tmW0,
-                const __grid_constant__ CUtensorMap tmW1, ThinMmaArgs args) {
+                const __grid_constant__ CUtensorMap tmW1,
+                const __grid_constant__ CUtensorMap tmXrow, ThinMmaArgs args) {
     using C = Cfg<kGated>;
     extern __shared__ uint8_t smem_raw[];
+    __shared__ SmallPlan sp;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
@@ -115,7 +126,27 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
     const uint32_t tmem_base = *tmem_holder;
     grid_dep_wait();      // everything above overlaps the previous kernel
     grid_dep_launch();
-    const int total = args.hdr_ro->n_thin_mma * args.n_blocks;   // CTAs past it idle
+    const bool self = args.sr.logits != nullptr;
+    if (self) {
+        if (kGated) {
+            build_small_plan(args.sr, sp);
+            if (blockIdx.x == 0) write_small_plan(args.sr, sp, args.hdr, true);
+        } else {
+            load_small_plan(args.sr, args.hdr, sp);
+        }
+    }
+    const int n_tiles = self ? sp.n_units : args.hdr_ro->n_thin_mma;
+    const int total = n_tiles * args.n_blocks;   // CTAs past it idle
+    auto tile_at = [&](int i) {
+        if (!self) return args.tiles[i];
+        const ThinUnit u = sp.units[i];
+        FatTile f;
+        f.expert = u.expert;
+        f.row0 = u.row0;
+        f.rows = u.n;
+        f.pad = 0;
+        return f;
+    };
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer ----------------
@@ -126,10 +157,10 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
         bool ok = true;
         // Each item's tile is loaded one item ahead (its latency is hidden).
         FatTile ft_next = {};
-        if ((int)blockIdx.x < total) ft_next = args.tiles[blockIdx.x / args.n_blocks];
+        if ((int)blockIdx.x < total) ft_next = tile_at(blockIdx.x / args.n_blocks);
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
             const FatTile ft = ft_next;
-            if (t + (int)gridDim.x < total) ft_next = args.tiles[(t + gridDim.x) / args.n_blocks];
+            if (t + (int)gridDim.x < total) ft_next = tile_at((t + gridDim.x) / args.n_blocks);
             const int wrow = weight_block(args.wslot, ft.expert) * args.w_rows_per_expert +
                              (t % args.n_blocks) * BM;
             for (int kb = 0; kb < args.k_blocks; ++kb) {
@@ -138,10 +169,18 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
                     break;
                 }
                 const uint32_t sw = base + stage * C::kStageBytes;
-                mbar_expect_tx(full_bar(stage), C::kStageBytes);
+                const bool rows = kGated && self;   // x rows by token, one box each
+                mbar_expect_tx(full_bar(stage), rows ? (uint32_t)(C::kMats * W_BYTES + ft.rows * BK * 2)
+                                                     : (uint32_t)C::kStageBytes);
                 tma_load_2d(sw, &tmW0, full_bar(stage), kb * BK, wrow);
                 if (kGated) tma_load_2d(sw + W_BYTES, &tmW1, full_bar(stage), kb * BK, wrow);
-                tma_load_2d(sw + C::kMats * W_BYTES, &tmX, full_bar(stage), kb * BK, ft.row0);
+                if (rows) {
+                    for (int j = 0; j < ft.rows; ++j)
+                        tma_load_2d(sw + C::kMats * W_BYTES + (uint32_t)(j * BK * 2), &tmXrow,
+                                    full_bar(stage), kb * BK, sp.perm[ft.row0 + j] / args.sr.k);
+                } else {
+                    tma_load_2d(sw + C::kMats * W_BYTES, &tmX, full_bar(stage), kb * BK, ft.row0);
+                }
                 pending[stage] = (int)phase;
                 if (++stage == C::kStages) {
                     stage = 0;
@@ -210,10 +249,10 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
         const int ew = warp - 4;   // TMEM lanes (weight rows) 32*ew .. 32*ew+31
         int it = 0;
         FatTile ft_next = {};
-        if ((int)blockIdx.x < total) ft_next = args.tiles[blockIdx.x / args.n_blocks];
+        if ((int)blockIdx.x < total) ft_next = tile_at(blockIdx.x / args.n_blocks);
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
             const FatTile ft = ft_next;
-            if (t + (int)gridDim.x < total) ft_next = args.tiles[(t + gridDim.x) / args.n_blocks];
+            if (t + (int)gridDim.x < total) ft_next = tile_at((t + gridDim.x) / args.n_blocks);
             const int acc = it & 1;
             if (*abort_flag || !mbar_wait(tfull_bar(acc), (uint32_t)((it >> 1) & 1))) {
                 *abort_flag = 1;
@@ -254,6 +293,7 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
         fence_after();
         tmem_dealloc(tmem_base, C::kTmemCols);
     }
+    if (!kGated && self && args.sr.out) combine_if_last(args.sr, sp, args.hdr, args.out, (int)args.ld_out);
 }
 
 template <bool kGated>
@@ -267,10 +307,13 @@ cudaError_t set_smem_attr() {
 cudaError_t launch_thin_mma_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_alloc,
                                     const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int H,
                                     int I, const Plan& plan, __nv_bfloat16* h, int num_sms,
-                                    cudaStream_t s) {
-    CUtensorMap mX, mG, mU;
+                                    cudaStream_t s, const SelfRoute* sr, const __nv_bfloat16* x) {
+    CUtensorMap mX, mG, mU, mXr;
     cudaError_t e;
     if ((e = make_tma_map_bf16(&mX, x_sorted, (uint64_t)rows_alloc, (uint64_t)H, BN)) != cudaSuccess) return e;
+    mXr = mX;
+    if (sr && (e = make_tma_map_bf16(&mXr, x, (uint64_t)sr->T, (uint64_t)H, 1)) != cudaSuccess)
+        return e;
     if ((e = make_tma_map_bf16(&mG, Wg, (uint64_t)plan.n_wblocks * I, (uint64_t)H, BM)) != cudaSuccess) return e;
     if ((e = make_tma_map_bf16(&mU, Wu, (uint64_t)plan.n_wblocks * I, (uint64_t)H, BM)) != cudaSuccess) return e;
     if ((e = set_smem_attr<true>()) != cudaSuccess) return e;
@@ -284,13 +327,15 @@ cudaError_t launch_thin_mma_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_
     a.w_rows_per_expert = I;
     a.out = h;
     a.ld_out = I;
+    a.sr = sr ? *sr : SelfRoute{};
     return launch_pdl(thin_mma_kernel<true>, dim3(num_sms), dim3(256), Cfg<true>::kSmemBytes, s,
-                      mX, mG, mU, a);
+                      mX, mG, mU, mXr, a);
 }
 
 cudaError_t launch_thin_mma_down(const __nv_bfloat16* h, int64_t rows_alloc,
                                  const __nv_bfloat16* Wd, int H, int I, const Plan& plan,
-                                 __nv_bfloat16* y_sorted, int num_sms, cudaStream_t s) {
+                                 __nv_bfloat16* y_sorted, int num_sms, cudaStream_t s,
+                                 const SelfRoute* sr) {
     CUtensorMap mX, mD;
     cudaError_t e;
     if ((e = make_tma_map_bf16(&mX, h, (uint64_t)rows_alloc, (uint64_t)I, BN)) != cudaSuccess) return e;
@@ -306,8 +351,9 @@ cudaError_t launch_thin_mma_down(const __nv_bfloat16* h, int64_t rows_alloc,
     a.w_rows_per_expert = H;
     a.out = y_sorted;
     a.ld_out = H;
+    a.sr = sr ? *sr : SelfRoute{};
     return launch_pdl(thin_mma_kernel<false>, dim3(num_sms), dim3(256), Cfg<false>::kSmemBytes, s,
-                      mX, mD, mD, a);
+                      mX, mD, mD, mX, a);
 }
 
 }  // namespace moe

@@ -141,12 +141,16 @@ def test_forward_launch_count(moe):
     down kernel: gate/up, down."""
     S = moe.Shape
     # decode: 8 or 16 touched experts x 16 blocks < 384 items -> CUDA cores,
-    # batch routed inside the streaming kernels
+    # from 24 x 16 = 384 on tensor cores; up to 32 slots the batch is routed
+    # inside the streaming kernels either way
     assert moe.forward_launches(S(1, 384, 8, 4096, 2048)) == 2
     assert moe.forward_launches(S(2, 384, 8, 4096, 2048)) == 2
-    assert moe.forward_launches(S(3, 384, 8, 4096, 2048)) == 6       # 24 x 16 = 384: tensor cores
-    assert moe.forward_launches(S(1, 384, 8, 4096, 2048, thin_mma_min=1)) == 6
+    assert moe.forward_launches(S(3, 384, 8, 4096, 2048)) == 2
+    assert moe.forward_launches(S(4, 384, 8, 4096, 2048)) == 2
+    assert moe.forward_launches(S(1, 384, 8, 4096, 2048, thin_mma_min=1)) == 2
     assert moe.forward_launches(S(4, 384, 8, 4096, 2048, thin_mma_min=33)) == 2
+    assert moe.forward_launches(S(4, 384, 8, 4096, 2048, thin_mma_min=3)) == 8   # split kernels
+    assert moe.forward_launches(S(8, 384, 8, 4096, 2048)) == 6       # 64 slots: planned
     # self-routing limits: 32 slots, below the fat threshold, one unit per expert
     assert moe.forward_launches(S(5, 384, 8, 4096, 2048, thin_mma_min=33)) == 5   # 40 slots
     assert moe.forward_launches(S(32, 64, 1, 512, 256, thin_mma_min=33)) == 10    # T = 32 may be fat

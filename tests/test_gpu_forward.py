@@ -143,9 +143,10 @@ def test_forward_threshold_edges(moe, mma_min):
     _full_check(moe, s2, 32, inp, mma_min=mma_min)
 
 
-# Small batches on the CUDA-core streaming kernels route themselves inside
-# them and combine in the down kernel (two launches): T*k <= 32, T below the
-# fat threshold and within one streaming unit.
+# Small batches route themselves inside the streaming kernels and combine in
+# the down kernel (two launches): T*k <= 32, T below the fat threshold, all
+# touched experts on the tensor-core kernel or all on the CUDA-core kernel
+# within one streaming unit.
 SELF_ROUTED = [
     # T, E, k, H, I
     (1, 16, 2, 512, 256),
@@ -158,17 +159,18 @@ SELF_ROUTED = [
 ]
 
 
+@pytest.mark.parametrize("mma_min", [MMA_NONE, MMA_ALL])
 @pytest.mark.parametrize("T,E,k,H,I", SELF_ROUTED)
-def test_forward_self_routed(moe, T, E, k, H, I):
+def test_forward_self_routed(moe, T, E, k, H, I, mma_min):
     """Routing bit-exact and outputs against the oracle; and bit-identical to
     the same batch through the separate entry points (router, route lists,
-    expert FFN on the planner's units, combine)."""
+    expert FFN on the planner's units or tiles, combine)."""
     s = synth.Shape(T=T, E=E, k=k, H=H, I=I)
     inp = synth.make_layer(s, seed=100 + T, zipf_s=synth.ZIPF_S)
     d = _to_dev(inp)
-    shape = moe.Shape(T, E, k, H, I, fat_threshold=32, thin_mma_min=MMA_NONE)
+    shape = moe.Shape(T, E, k, H, I, fat_threshold=32, thin_mma_min=mma_min)
     assert moe.forward_launches(shape) == 2
-    _full_check(moe, s, 32, inp, d, mma_min=MMA_NONE)
+    _full_check(moe, s, 32, inp, d, mma_min=mma_min)
     out, idx, gates = _forward(moe, shape, d)
     idx2, gates2 = moe.moe_route(d["logits"], k)
     counts, offsets, perm, inv = moe.moe_permute(idx2, E)
