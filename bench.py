@@ -183,6 +183,10 @@ def stage_work(shape, counts_np):
     # tensor-core streaming kernel (the library's rule when thin_mma_min is 0)
     mma_min = shape.thin_mma_min or (1 if min(E, P) * (I // 128) >= 384 else 33)
     mma_rows = int(counts_np[thin & (counts_np >= mma_min)].sum())
+    # batches of <= 32 slots below the fat threshold on the tensor-core kernel
+    # route themselves and load x rows directly: no gather
+    if P <= 32 and T < thr and mma_min <= 1:
+        mma_rows = 0
     n_fat, n_thin = int(fat.sum()), int(thin.sum())
     w_gu = 2 * I * H * 2      # gate + up bytes per expert
     w_d = H * I * 2
