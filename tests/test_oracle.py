@@ -304,3 +304,24 @@ def test_combine_one_hot_gates_select_rows():
     a = oracle.combine(y, inv, g2)
     b = oracle.combine(y, inv, 2.0 * g2)
     assert np.allclose(b, 2.0 * a, rtol=1e-15, atol=0)
+
+
+def test_workload_expert_mix():
+    """The seeded prefill chunk (16,384 tokens, 384 experts, top-8, Zipf(1.1)
+    router bias) routes to 233 experts: 81 fat ones (>= 32 slots) holding
+    130,162 slots and 152 thin ones holding 910; the decode sweep's 4 layers x
+    4 logit sets touch 8 / 12.19 / 17.63 / 24.63 / 32.81 / 38.5 experts on
+    average at batch 1 / 2 / 4 / 8 / 16 / 24 (the figures the benchmark and
+    its roofline bytes quote)."""
+    s = synth.PREFILL
+    idx, _ = oracle.route(synth.make_logits(s.T, s.E, seed=0, zipf_s=synth.ZIPF_S).numpy(), s.k)
+    c = np.bincount(idx.reshape(-1), minlength=s.E)
+    fat, thin = c >= 32, (c > 0) & (c < 32)
+    assert (c > 0).sum() == 233 and fat.sum() == 81 and thin.sum() == 152
+    assert c[fat].sum() == 130162 and c[thin].sum() == 910
+    expect = {1: 8.0, 2: 12.1875, 4: 17.625, 8: 24.625, 16: 32.8125, 24: 38.5}
+    for B in synth.DECODE_SWEEP_BATCHES:
+        touched = [len(np.unique(oracle.route(
+            synth.make_logits(B, s.E, seed=0, layer=l, rep=r, zipf_s=synth.ZIPF_S).numpy(),
+            s.k)[0])) for l in range(4) for r in range(4)]
+        assert np.mean(touched) == expect[B], B
