@@ -39,6 +39,11 @@
 //   down:    y[p, r] = bf16( Wd[e,r,:] . h[p, :] )
 // for every sorted position p of expert e (token t = perm[p] / k).
 //
+// Small batches (at most 32 slots, one unit per expert) route themselves: the
+// gate/up kernel builds the plan in every CTA and CTA 0 stores it, the down
+// kernel reads it back after its wait and its last CTA combines the batch
+// (small_plan.cuh).
+//
 // Waits are bounded; on expiry the kernel records MOE_ERR_TIMEOUT, the
 // producer waits (bounded) for its outstanding copies, and the CTA returns.
 #include <algorithm>
