@@ -306,6 +306,44 @@ def test_combine_one_hot_gates_select_rows():
     assert np.allclose(b, 2.0 * a, rtol=1e-15, atol=0)
 
 
+def test_combine_adds_its_terms():
+    # Partition of unity: every sorted row is the constant vector 1 and the
+    # gates are a softmax over the selection, so the combine is sum_j g_j = 1
+    # for every token.  A combine that kept one term (the largest gate, the
+    # first one) or averaged them would give max g < 1 or 1/k instead.
+    rng = np.random.default_rng(5)
+    T, E, k, H = 40, 12, 4, 7
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    _, gates = oracle.route(lg, k)
+    assert gates.max(axis=1).max() < 0.99 and np.abs(gates.sum(1) - 1).max() < 1e-12
+    inv = rng.permutation(T * k).astype(np.int32)
+    out = oracle.combine(np.ones((T * k, H)), inv, gates)
+    assert np.allclose(out, 1.0, rtol=0, atol=1e-14)
+
+
+def test_combine_of_expert_rows_is_the_layer():
+    # The combine, fed the sorted expert outputs of a routed layer (each slot's
+    # row from the expert FFN, placed by the route lists), gives the layer
+    # output that oracle.moe_tokens computes token by token -- the function
+    # pinned above by the dense SwiGLU (E=1), the two-expert closed form and
+    # the hand-worked layer.  A combine that dropped, maxed or reordered
+    # terms, or read the wrong sorted row, would miss it.
+    shape = synth.Shape(T=16, E=6, k=3, H=64, I=32)
+    inp = synth.make_layer(shape, seed=9, zipf_s=1.1)
+    xb = synth.bf16_bits(inp["x"])
+    lg = inp["logits"].numpy()
+    W = [tuple(synth.bf16_bits(w[e]) for w in (inp["Wg"], inp["Wu"], inp["Wd"]))
+         for e in range(shape.E)]
+    ref, idx, gates = oracle.moe_tokens(xb, lg, shape.k, W)
+    counts, offsets, perm, inv = oracle.permute(idx, shape.E)
+    y_sorted = np.empty((shape.P, shape.H))
+    for p, s in enumerate(perm):
+        t, j = divmod(int(s), shape.k)
+        y_sorted[p] = oracle.expert_ffn(xb[t], *W[idx[t, j]])[1]
+    out = oracle.combine(y_sorted, inv, gates)
+    assert np.allclose(out, ref, rtol=0, atol=1e-13 * np.abs(ref).max())
+
+
 def test_workload_expert_mix():
     """The seeded prefill chunk (16,384 tokens, 384 experts, top-8, Zipf(1.1)
     router bias) routes to 233 experts: 81 fat ones (>= 32 slots) holding
