@@ -5,8 +5,9 @@ Headline workload: one MoE layer over a 16,384-token prefill chunk (384
 experts, top-8, H=4096, I=2048, bf16, Zipf(1.1)-skewed router logits, fat
 threshold 32).  A step is one moe_forward: route, route lists, both expert
 paths and the combine.  Reported beside it: decode batches 1 and 4 on the
-same layer, the decode batch sweep 1..24 over 4 resident layers, and (with
---offload) the 12-layer prefill streamed from pinned host memory.
+same layer, the decode batch sweep 1..24 over 4 resident layers, and (unless
+--no-offload) the 12-layer prefill streamed from pinned host memory with the
+host link's own copy bandwidth beside it.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 
@@ -208,6 +209,13 @@ def stage_work(shape, counts_np):
     }
 
 
+# Nominal GB300 figures (dense bf16 tensor rate, HBM3e bandwidth): the
+# targets are stated against these, so every fraction of the measured peaks
+# is reported beside its fraction of the nominal ones.
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 8000.0
+
+
 def roofline_for(stage, work, ms, peaks):
     w = work[stage]
     if stage.startswith("gemm"):
@@ -217,11 +225,13 @@ def roofline_for(stage, work, ms, peaks):
         peak = peaks["bf16_tflops"]
         return {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(ach / peak, 4),
-                "peak_note": f"bf16 dense burst (cuBLAS), {peaks['source']}"}
+                "peak_note": f"bf16 dense burst (cuBLAS), {peaks['source']}",
+                "frac_nominal": round(ach / NOMINAL_BF16_TFLOPS, 4)}
     ach = w["bytes"] / (ms * 1e-3) / 1e9
     peak = peaks["hbm_gbs"]
     return {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(ach / peak, 4), "peak_note": f"HBM copy, {peaks['source']}"}
+            "frac": round(ach / peak, 4), "peak_note": f"HBM copy, {peaks['source']}",
+            "frac_nominal": round(ach / NOMINAL_HBM_GBS, 4)}
 
 
 class Layer:
@@ -366,6 +376,21 @@ def oracle_sample(n_tokens, expert_source, logits_np, x_bits, k, seed=123):
     return n_tokens / dt, dt, len(need)
 
 
+def prefill_config(T, E, info, thin_mma_min, world):
+    """The bench line's config (both arms print the same one)."""
+    return {
+        "workload": f"prefill chunk: 1 MoE layer, T={T} tokens, E={E} experts, top-8, "
+                    "H=4096, I=2048, bf16, Zipf(1.1) router bias, fat threshold 32",
+        "parallelism": "replicas only" if world > 1 else "single GPU",
+        "l2": f"inputs larger than L2 ({E * 3 * 4096 * 2048 * 2 / 1e9:.1f} GB of expert "
+              "weights per layer)",
+        "fat_experts": info["fat_experts"],
+        "thin_experts": info["thin_experts"],
+        "touched_experts": info["touched"],
+        "thin_mma_min": thin_mma_min or "default",
+    }
+
+
 def run_reference(args):
     """--impl reference: the oracle as it stands, on the host cores, each step
     a bounded token sample of the prefill workload."""
@@ -383,6 +408,14 @@ def run_reference(args):
             cache[e] = tuple(synth.bf16_bits(w) for w in synth.make_expert(e, shape.H, shape.I))
         return cache[e]
 
+    # the workload's expert mix, as the GPU arm's config states it
+    import oracle
+    oracle.build()
+    idx, _ = oracle.route(logits_np, shape.k)
+    counts = np.bincount(idx.reshape(-1), minlength=shape.E)
+    fat, thin = counts >= FAT_THRESHOLD, (counts > 0) & (counts < FAT_THRESHOLD)
+    info = dict(fat_experts=int(fat.sum()), thin_experts=int(thin.sum()),
+                touched=int((counts > 0).sum()))
     times = []
     for i in range(args.warmup + args.steps):
         tps, dt, _ = oracle_sample(tokens_per_step, expert, logits_np, x_bits, shape.k, seed=i)
@@ -395,11 +428,9 @@ def run_reference(args):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * total / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "prefill chunk: T=16384, E=384, top-8, H=4096, I=2048, "
-                               "Zipf(1.1) router bias (oracle on a token sample)",
-                   "tokens_per_step": tokens_per_step},
+        "config": prefill_config(shape.T, shape.E, info, 0, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": 1,
-                         "kind": "oracle",
+                         "host_cores": os.cpu_count(), "kind": "oracle",
                          "sample": f"{tokens_per_step} tokens per step of the 16,384-token "
                                    "chunk, all of their 8 experts each, single-threaded fp64"},
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -463,6 +494,7 @@ def run_sweep(moe, dev, base_weights, peaks, thin_mma_min=0, reps=40, warmup=5, 
             "us_per_step": round(1e3 * ms, 2),
             "touched_experts_per_layer": round(sum(touched) / len(touched), 2),
             "frac_of_hbm_roofline": round(bytes_step / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "frac_of_nominal_hbm": round(bytes_step / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
         }
         del graphs, ws
     del layers[1:]
@@ -471,6 +503,27 @@ def run_sweep(moe, dev, base_weights, peaks, thin_mma_min=0, reps=40, warmup=5, 
 
 
 # --------------------------------------------------------------- offload
+
+def measure_h2d_link(dev, nbytes=1 << 31, reps=5):
+    """Host-to-device copy bandwidth of this box's link (GB/s): one copy of
+    nbytes from pinned host memory, best of reps, CUDA events on a side
+    stream (what the stager's copies can reach at most)."""
+    src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    src.fill_(1)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    st = torch.cuda.Stream(device=dev)
+    best = float("inf")
+    with torch.cuda.stream(st):
+        for _ in range(reps + 1):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            dst.copy_(src, non_blocking=True)
+            b.record(st)
+            b.synchronize()
+            best = min(best, a.elapsed_time(b))
+    del src, dst
+    return nbytes / (best * 1e-3) / 1e9
+
 
 def run_offload(args, moe, dev, n_layers=12, n_slots=8):
     """Offload prefill: 12 layers x 384 experts (H=2048, I=1024, bf16, 58 GB)
@@ -528,6 +581,8 @@ def run_offload(args, moe, dev, n_layers=12, n_slots=8):
         touched.append(int(torch.unique(idx).numel()))
     per_expert = moe.layer_weight_bytes(shape) // s.E
     copied = sum(touched) * per_expert
+    link = measure_h2d_link(dev)
+    h2d = copied / (ms * 1e-3) / 1e9
     return {
         "workload": "12 MoE layers x 384 experts, H=2048, I=1024, bf16 (58 GB pinned host), "
                     "8 HBM staging slots, T=16384, top-8, Zipf(1.1)",
@@ -535,7 +590,10 @@ def run_offload(args, moe, dev, n_layers=12, n_slots=8):
         "ms_per_chunk": round(ms, 3),
         "touched_experts_per_layer": round(sum(touched) / n_layers, 1),
         "h2d_bytes_per_chunk": copied,
-        "h2d_gbs": round(copied / (ms * 1e-3) / 1e9, 1),
+        "h2d_gbs": round(h2d, 1),
+        "link_h2d_gbs": round(link, 1),
+        "frac_of_link": round(h2d / link, 4),
+        "link_note": "one 2 GiB pinned-host-to-device copy, best of 5, CUDA events",
         "compute_ms_per_layer_resident": round(layer_ms, 3),
         "bound": "host-to-device copy" if ms > n_layers * layer_ms * 1.2 else "compute",
         "decode_with_expert_cache": cached,
@@ -638,7 +696,7 @@ def run_gpu(args):
     stages = {s: {"ms": round(stage_ms[s], 4), **{k2: v2 for k2, v2 in
                                                  roofline_for(s, work, max(stage_ms[s], 1e-6),
                                                               peaks).items()
-                                                 if k2 in ("achieved", "unit", "frac")}}
+                                                 if k2 in ("achieved", "unit", "frac", "frac_nominal")}}
               for s in stage_ms}
     layer_ideal_ms = max(
         (work["gemm_gate_up"]["flops"] + work["gemm_down"]["flops"]
@@ -720,6 +778,8 @@ def run_gpu(args):
                 "touched_experts": dwork["_info"]["touched"],
                 "layer_frac_of_hbm_roofline": round(
                     bytes_step / (gt / reps * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                "layer_frac_of_nominal_hbm": round(
+                    bytes_step / (gt / reps * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
                 "stage_us_eager": {s: round(1e3 * v, 2) for s, v in dst.items()},
             }
             del dl
@@ -732,7 +792,8 @@ def run_gpu(args):
         n = args.cpu_tokens
         tps, dt, n_exp = oracle_sample(n, expert, layer.logits_cpu[0].numpy(),
                                        synth.bf16_bits(layer.x_cpu), shape.k)
-        cpu = {"value": round(tps, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        cpu = {"value": round(tps, 4), "unit": "tokens/s", "cores": 1,
+               "host_cores": os.cpu_count(), "kind": "oracle",
                "sample": f"{n} tokens of the 16,384-token chunk with all their experts "
                          f"({n * shape.k} token-expert pairs, {n_exp} experts), "
                          f"single-threaded fp64, {dt:.1f} s"}
@@ -740,7 +801,11 @@ def run_gpu(args):
     sweep = None
     if not args.no_sweep:
         sweep = run_sweep(moe, dev, (layer.Wg, layer.Wu, layer.Wd), peaks, args.thin_mma_min)
-    offload = run_offload(args, moe, dev) if args.offload else None
+    # One replica's offload leg pins 58 GB of host memory, so it runs at N=1 only.
+    offload = None
+    if not (args.no_offload or args.tokens or args.experts):
+        offload = run_offload(args, moe, dev) if world == 1 else {
+            "skipped": "runs at N=1 only (58 GB of pinned host memory per replica)"}
 
     launches = moe.forward_launches(shape) * args.steps
     if rank == 0:
@@ -749,17 +814,7 @@ def run_gpu(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {
-                "workload": f"prefill chunk: 1 MoE layer, T={T} tokens, E={E} experts, top-8, "
-                            "H=4096, I=2048, bf16, Zipf(1.1) router bias, fat threshold 32",
-                "parallelism": "replicas only" if world > 1 else "single GPU",
-                "l2": f"inputs larger than L2 ({E * 3 * 4096 * 2048 * 2 / 1e9:.1f} GB of expert "
-                      "weights per layer)",
-                "fat_experts": work["_info"]["fat_experts"],
-                "thin_experts": work["_info"]["thin_experts"],
-                "touched_experts": work["_info"]["touched"],
-                "thin_mma_min": shape.thin_mma_min or "default",
-            },
+            "config": prefill_config(T, E, work["_info"], shape.thin_mma_min, world),
             "roofline": roof,
             "layer_roofline": {"ideal_ms": round(layer_ideal_ms, 4),
                                "frac": round(layer_ideal_ms / ms_per_step, 4),
@@ -817,8 +872,8 @@ def main():
                     help="override E of the layer (small cases for profiling)")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the decode batch sweep over 4 resident layers")
-    ap.add_argument("--offload", action="store_true",
-                    help="also run the offload prefill (58 GB of experts in pinned host memory)")
+    ap.add_argument("--no-offload", action="store_true",
+                    help="skip the offload prefill (58 GB of experts in pinned host memory)")
     ap.add_argument("--thin-mma-min", type=int, default=0,
                     help="slots from which a thin expert streams on the tensor cores "
                          "(0: library default; 33: CUDA cores only)")

@@ -300,8 +300,13 @@ def layer_weight_bytes(shape: Shape) -> int:
 def pack_layer_weights(W_gate, W_up, W_down, pin: bool = True) -> torch.Tensor:
     """One layer's experts as the contiguous W_gate | W_up | W_down block the
     stager copies (pinned host memory by default)."""
-    flat = torch.cat([W_gate.reshape(-1), W_up.reshape(-1), W_down.reshape(-1)]).cpu()
-    return flat.pin_memory() if pin else flat
+    parts = [W_gate.reshape(-1), W_up.reshape(-1), W_down.reshape(-1)]
+    out = torch.empty(sum(p.numel() for p in parts), dtype=torch.bfloat16, pin_memory=pin)
+    off = 0
+    for p in parts:   # straight into the (pinned) block, no intermediate copy
+        out[off:off + p.numel()].copy_(p)
+        off += p.numel()
+    return out
 
 
 class Stager:
