@@ -58,3 +58,37 @@ def oracle_rows(x_bits, logits_np, k, experts, tokens):
     tokens = np.asarray(tokens, dtype=np.int64)
     out, idx, gates = oracle.moe_tokens(x_bits[tokens], logits_np[tokens], k, experts)
     return out, idx, gates
+
+
+def sample_tokens(idx_np, counts_np, thr, rng, n_random=24, hot_tiles=32):
+    """Token ids for an oracle check of a large layer: random tokens, tokens
+    of thin experts, of the smallest and the hottest fat expert, and of
+    experts holding exactly 31/32/33 slots (the fat-threshold boundary).
+    The hottest expert also gets one token in each of up to `hot_tiles`
+    evenly spaced 256-row pair tiles of its sorted rows, at a different row
+    of each tile, so a tile- or row-indexing fault anywhere in the grouped
+    GEMM shows."""
+    T = idx_np.shape[0]
+    picks = set(rng.choice(T, size=min(n_random, T), replace=False).tolist())
+    thin = np.where((counts_np > 0) & (counts_np < thr))[0]
+    fat = np.where(counts_np >= thr)[0]
+    thin_tokens = np.where(np.isin(idx_np, thin).any(1))[0]
+    picks.update(rng.choice(thin_tokens, size=min(8, len(thin_tokens)), replace=False).tolist())
+    if len(fat):
+        smallest = fat[np.argmin(counts_np[fat])]
+        hottest = fat[np.argmax(counts_np[fat])]
+        for e in (smallest, hottest):
+            toks = np.where((idx_np == e).any(1))[0]
+            picks.update(toks[:3].tolist())
+    for c in (31, 32, 33):
+        for e in np.where(counts_np == c)[0][:1]:
+            picks.update(np.where((idx_np == e).any(1))[0][:2].tolist())
+    if len(fat) and hot_tiles:
+        hottest = fat[np.argmax(counts_np[fat])]
+        # the expert's slots in sorted order (ascending slot id), 256 per tile
+        slots = np.flatnonzero(idx_np.reshape(-1) == hottest)
+        n_tiles = (len(slots) + 255) // 256
+        for q in np.unique(np.linspace(0, n_tiles - 1, min(hot_tiles, n_tiles)).astype(int)):
+            r = min(256 * q + (53 * q) % 256, len(slots) - 1)
+            picks.add(int(slots[r]) // idx_np.shape[1])
+    return np.array(sorted(picks))

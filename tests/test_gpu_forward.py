@@ -213,6 +213,36 @@ def test_forward_self_routed_ties_and_reuse(moe):
     assert_close(out, ref, "self-routed ties")
 
 
+@pytest.mark.parametrize("mma_min", [MMA_NONE, MMA_ALL])
+def test_forward_self_routed_back_to_back(moe, mma_min):
+    """Self-routed decode steps of batch 1, 2 and 4 enqueued back to back on
+    one workspace with no synchronisation between them (programmatic
+    dependent launch on): every step's fused combine counts its down CTAs on
+    the same ticket word, so a ticket left behind by one step would make the
+    next step combine early or not at all.  Each step against the oracle."""
+    E, k, H, I = 64, 8, 1024, 512
+    Wg, Wu, Wd = synth.make_weights(E, H, I, seed=21, layer=0, device="cuda")
+    experts = DeviceExperts(Wg, Wu, Wd)
+    batches = [1, 2, 4, 4, 1, 2, 1, 4]
+    shapes = {B: moe.Shape(B, E, k, H, I, fat_threshold=32, thin_mma_min=mma_min)
+              for B in set(batches)}
+    for sh in shapes.values():
+        assert moe.forward_launches(sh) == 2
+    ws = moe.Workspace(max(moe.workspace_size(sh) for sh in shapes.values()))
+    steps = []
+    for r, B in enumerate(batches):
+        x = synth.make_x(B, H, seed=200 + r)
+        lg = synth.make_logits(B, E, seed=200 + r, zipf_s=synth.ZIPF_S)
+        out = moe.moe_forward(shapes[B], lg.cuda(), x.cuda(), Wg, Wu, Wd, ws=ws)
+        steps.append((x, lg, out))
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    for r, (x, lg, out) in enumerate(steps):
+        ref, _, _ = oracle_rows(synth.bf16_bits(x), lg.numpy(), k, experts,
+                                np.arange(x.shape[0]))
+        assert_close(out, ref, f"step {r} (B={x.shape[0]})")
+
+
 def test_forward_gemm_pair_boundaries(moe):
     """The grouped GEMM runs an expert's 128-row tiles in pairs (256 rows per
     CTA pair): slot counts on either side of pair and tile boundaries, so
@@ -276,25 +306,6 @@ def test_forward_decode(moe, big_layer, B, mma_min):
     _full_check(moe, s, 32, inp, d, mma_min=mma_min)
 
 
-def _sample_tokens(idx_np, counts_np, thr, rng, n_random=24):
-    T = idx_np.shape[0]
-    picks = set(rng.choice(T, size=min(n_random, T), replace=False).tolist())
-    thin = np.where((counts_np > 0) & (counts_np < thr))[0]
-    fat = np.where(counts_np >= thr)[0]
-    thin_tokens = np.where(np.isin(idx_np, thin).any(1))[0]
-    picks.update(rng.choice(thin_tokens, size=min(8, len(thin_tokens)), replace=False).tolist())
-    if len(fat):
-        smallest = fat[np.argmin(counts_np[fat])]
-        hottest = fat[np.argmax(counts_np[fat])]
-        for e in (smallest, hottest):
-            toks = np.where((idx_np == e).any(1))[0]
-            picks.update(toks[:3].tolist())
-    for c in (31, 32, 33):
-        for e in np.where(counts_np == c)[0][:1]:
-            picks.update(np.where((idx_np == e).any(1))[0][:2].tolist())
-    return np.array(sorted(picks))
-
-
 @pytest.mark.parametrize("H,I,mma_min", [(4096, 2048, 0), (4096, 2048, MMA_NONE),
                                          (2048, 1024, 0)])
 def test_forward_prefill_sampled(moe, big_layer, H, I, mma_min):
@@ -322,7 +333,7 @@ def test_forward_prefill_sampled(moe, big_layer, H, I, mma_min):
     assert np.array_equal(counts.cpu().numpy(), rc) and np.array_equal(perm.cpu().numpy(), rp)
     assert np.array_equal(inv.cpu().numpy(), ri)
     assert (rc >= 32).sum() > 0 and ((rc > 0) & (rc < 32)).sum() > 0
-    toks = _sample_tokens(ridx, rc, 32, np.random.default_rng(1))
+    toks = sample_tokens(ridx, rc, 32, np.random.default_rng(1))
     experts = DeviceExperts(W["Wg"], W["Wu"], W["Wd"])
     ref, _, _ = oracle_rows(synth.bf16_bits(inp["x"]), lg, s.k, experts, toks)
     assert_close(out[torch.from_numpy(toks).cuda()], ref, f"prefill H={H} mma_min={mma_min}")
