@@ -149,9 +149,9 @@ __device__ inline void load_small_plan(const SelfRoute& sr, const WsHeader* hdr,
 // The last CTA of a streaming down kernel to finish combines the batch.
 // Called by every thread of the block once its y rows are stored: each
 // thread fences its stores, the CTA takes a ticket from the workspace header
-// (zeroed by the gate/up kernel), and the CTA with the last ticket reads
-// every CTA's rows (through L2) and writes out.  No thread waits on another
-// CTA.
+// (zeroed by the gate/up kernel, and again by the CTA that takes the last
+// ticket), and the CTA with the last ticket reads every CTA's rows (through
+// L2) and writes out.  No thread waits on another CTA.
 __device__ inline void combine_if_last(const SelfRoute& sr, const SmallPlan& sp, WsHeader* hdr,
                                        const __nv_bfloat16* y_sorted, int H);
 
@@ -182,7 +182,13 @@ __device__ inline void combine_if_last(const SelfRoute& sr, const SmallPlan& sp,
     __shared__ int s_last;
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(&hdr->ticket, 1) == (int)gridDim.x - 1;
+    if (threadIdx.x == 0) {
+        s_last = atomicAdd(&hdr->ticket, 1) == (int)gridDim.x - 1;
+        // Every CTA has taken its ticket: the last one sets the counter back
+        // to zero at once, so a step never leaves a count behind for the
+        // next one (whose gate/up kernel zeroes it as well).
+        if (s_last) atomicExch(&hdr->ticket, 0);
+    }
     __syncthreads();
     if (s_last) {
         __threadfence();
