@@ -133,7 +133,10 @@ moe_status moe_permute(const int32_t* topk_idx, int32_t T, int32_t E, int32_t k,
  *   - nothing is allocated: no cudaMalloc/cudaFree, no allocating library
  *     call; the first call on each device looks the array's device address
  *     up (cudaGetSymbolAddress, that device current) -- make that first call
- *     before any stream capture;
+ *     before any stream capture.  After a device reset (cudaDeviceReset) the
+ *     next call on that device finds a new context and looks it up again, so
+ *     make that call before any capture too;
+ *   - device ordinals 0..63 only (MOE_ERR_UNSUPPORTED beyond);
  *   - all calls share the array and it keeps the last call's contents; each
  *     call clears the status it needs.  Calls that overlap on the GPU (e.g.
  *     on unordered streams) race and give wrong results.

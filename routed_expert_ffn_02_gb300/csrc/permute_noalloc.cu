@@ -21,6 +21,10 @@
 //     it names a host-side shadow).  The device address is looked up once per
 //     device with cudaGetSymbolAddress, with that device current, by the
 //     first call made on it; make that first call before any stream capture.
+//     A device reset (cudaDeviceReset) ends the context that address belongs
+//     to: the next call on that device sees a new context and looks the
+//     address up again (the lookup is keyed by the context's unique id).
+#include <cuda.h>
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -28,6 +32,34 @@
 using namespace moe;
 
 namespace {
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (0 if there is none).
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
 constexpr int64_t kNoallocMaxSlots = 262144;   // T * k
 constexpr int64_t kNoallocMaxChunks = kNoallocMaxSlots / kPermChunk;
@@ -39,6 +71,7 @@ static __device__ __align__(256) unsigned char g_permute_scratch[kScratchBytes];
 
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};   // context id of the address
 
 }  // namespace
 
@@ -61,16 +94,21 @@ extern "C" moe_status moe_permute_noalloc(const int32_t* topk_idx, int32_t T, in
         return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
 
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-        return fail(MOE_ERR_CUDA, "cudaGetDevice failed");
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaGetDevice failed");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(MOE_ERR_UNSUPPORTED, "device ordinal beyond the 64 devices it keeps scratch "
+                                         "addresses for");
     void* base = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        if (!g_scratch_addr[dev]) {
+        const unsigned long long ctx = current_context_id();
+        if (!g_scratch_addr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
             void* p = nullptr;
             const cudaError_t e = cudaGetSymbolAddress(&p, g_permute_scratch);
             if (e != cudaSuccess || !p) return fail(MOE_ERR_CUDA, cudaGetErrorString(e));
             g_scratch_addr[dev] = p;
+            // the lookup made the device's context current if it was not yet
+            g_scratch_ctx[dev] = ctx ? ctx : current_context_id();
         }
         base = g_scratch_addr[dev];
     }

@@ -40,7 +40,8 @@ def _call_noalloc(moe, idx, E, out, status):
     assert st == 0, lib.moe_last_error()
 
 
-@pytest.mark.parametrize("T,E,k", [(4, 384, 8), (16384, 384, 8), (3000, 1024, 3)])
+@pytest.mark.parametrize("T,E,k", [(4, 384, 8), (16384, 384, 8), (3000, 1024, 3),
+                                   (32768, 1024, 8)])   # the last fills the array
 def test_noalloc_matches_moe_permute_twice(moe, T, E, k):
     status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
     for call in range(2):
@@ -77,3 +78,21 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(moe):
     st = lib.moe_permute_noalloc(None, 262144 // 8 + 1, 384, 8, None, None, None, None, None,
                                  None)
     assert st == 2 and b"262144" in lib.moe_last_error()
+
+
+def test_noalloc_shape_changes_between_calls(moe):
+    """A call over the whole array (128 chunks of 2048 slots, E = 1024) and
+    then smaller multi-chunk calls with other E and chunk counts: each result
+    is bit-exact, so nothing of the previous call's histograms leaks in."""
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    for i, (T, E, k) in enumerate([(32768, 1024, 8), (5000, 48, 4), (20000, 700, 6),
+                                   (1, 1, 1), (9000, 1024, 2)]):
+        lg = synth.make_logits(T, E, seed=70 + i, zipf_s=synth.ZIPF_S).cuda()
+        idx, _ = moe.moe_route(lg, k)
+        ref = moe.moe_permute(idx, E)
+        got = _outs(T, E, k)
+        _call_noalloc(moe, idx, E, got, status)
+        torch.cuda.synchronize()
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b), (T, E, k)
+        assert status.item() == 0
