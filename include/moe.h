@@ -366,6 +366,21 @@ moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
  * fails).  The status is sticky; clear != 0 resets it to MOE_OK. */
 moe_status moe_workspace_status(void* ws, moe_stream_t stream, int32_t clear);
 
+/* Test hook for the timeout path (the pages' fail-loud guards, engram
+ * prestage page: a failure is reported, never hidden).  Every mbarrier wait
+ * in the main loops of the expert kernels (grouped GEMMs, both weight-
+ * streaming kernels) gives up after a bounded number of SM cycles -- by
+ * default about 2 s -- and the kernel then records MOE_ERR_TIMEOUT in the
+ * workspace status, stops issuing work, waits with that default bound for
+ * every copy and MMA it has issued, frees its tensor memory and returns.
+ * This call sets the main-loop bound of the calling thread's later launches
+ * to `cycles` (> 0), or restores the default (0); the drain waits keep the
+ * default.  With a short bound the kernels give up on waits that would have
+ * completed: the outputs of those launches are unspecified and the status
+ * reads MOE_ERR_TIMEOUT.  MOE_ERR_INVALID_ARG for cycles < 0.  Nothing else
+ * changes; it is meant for tests of the timeout path only. */
+moe_status moe_debug_set_wait_limit(int64_t cycles);
+
 /* Message for the last error returned to the calling thread ("" if none). */
 const char* moe_last_error(void);
 

@@ -11,4 +11,5 @@ from .binding import (  # noqa: F401
     expert_ffn_workspace_size, version, LIB_PATH, EXPORTED,
     PROFILE_EVENTS, PROFILE_STAGES, forward_launches, Stager, layer_weight_bytes,
     pack_layer_weights, Pipe, pipe_workspace_size, DecodeGraph, ExpertCache,
+    debug_set_wait_limit,
 )

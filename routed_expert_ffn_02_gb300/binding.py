@@ -39,7 +39,7 @@ EXPORTED = ("moe_route", "moe_permute_workspace_size", "moe_permute", "moe_permu
             "moe_workspace_status", "moe_last_error", "moe_version",
             "moe_pipe_workspace_size", "moe_pipe_create", "moe_pipe_destroy",
             "moe_forward_host", "moe_cache_bytes", "moe_cache_create", "moe_cache_destroy",
-            "moe_cache_stats", "moe_forward_cached")
+            "moe_cache_stats", "moe_forward_cached", "moe_debug_set_wait_limit")
 
 
 class MoeShape(ctypes.Structure):
@@ -110,6 +110,7 @@ _sig = {
     "moe_pipe_destroy": ([_P], _i32),
     "moe_forward_host": ([_P, _SP, _P, _P, _P, _P, _P, _P, _P, _sz, _P, _P, _P], _i32),
     "moe_workspace_status": ([_P, _P, _i32], _i32),
+    "moe_debug_set_wait_limit": ([ctypes.c_int64], _i32),
     "moe_last_error": ([], ctypes.c_char_p),
     "moe_version": ([], ctypes.c_char_p),
 }
@@ -143,6 +144,13 @@ def _check(status: int, where: str):
 
 def version() -> str:
     return _lib.moe_version().decode()
+
+
+def debug_set_wait_limit(cycles: int) -> None:
+    """Test hook (moe_debug_set_wait_limit): main-loop waits of this thread's
+    later expert-kernel launches give up after `cycles` SM cycles (0: the
+    default bound).  Only for tests of the timeout path."""
+    _check(_lib.moe_debug_set_wait_limit(int(cycles)), "moe_debug_set_wait_limit")
 
 
 class Workspace:

@@ -9,10 +9,16 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include "moe_internal.cuh"
+#include "ptx.cuh"
 
 using namespace moe;
 
 thread_local bool moe::t_pdl = false;
+thread_local long long moe::t_wait_cycles = 0;
+
+long long moe::main_wait_cycles() {
+    return t_wait_cycles > 0 ? t_wait_cycles : ptx::kWaitCycles;
+}
 
 namespace {
 
@@ -557,6 +563,12 @@ int32_t moe_forward_launches(const moe_shape* shape) {
     if (kn.mma) n += 2;                              // tensor-core streaming
     n += 1;                                          // combine
     return n;
+}
+
+moe_status moe_debug_set_wait_limit(int64_t cycles) {
+    if (cycles < 0) return fail(MOE_ERR_INVALID_ARG, "cycles = %lld < 0", (long long)cycles);
+    t_wait_cycles = (long long)cycles;
+    return ok();
 }
 
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {

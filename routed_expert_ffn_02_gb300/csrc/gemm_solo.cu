@@ -52,6 +52,7 @@ struct SoloArgs {
     int bn_out;            // output columns per tile (128 gated, 256 down)
     __nv_bfloat16* out;    // [rows, ld_out]
     int64_t ld_out;
+    long long wait_cycles;     // limit of each main-loop wait (SM cycles)
 };
 
 template <bool kGated>
@@ -119,7 +120,7 @@ grouped_gemm_solo_kernel(const __grid_constant__ CUtensorMap tmA,
             const int brow = weight_block(args.wslot, ft.expert) * args.b_rows_per_expert +
                              (t % args.n_blocks_n) * b_tile_rows;
             for (int kb = 0; kb < args.k_blocks; ++kb) {
-                if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
+                if (!mbar_wait_for(empty_bar(stage), phase ^ 1u, args.wait_cycles, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -155,14 +156,14 @@ grouped_gemm_solo_kernel(const __grid_constant__ CUtensorMap tmA,
         bool issued = false;
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++it) {
             const int acc = it & 1;
-            if (*abort_flag || !mbar_wait(tempty_bar(acc), (uint32_t)((it >> 1) & 1) ^ 1u)) {
+            if (!mbar_wait_for(tempty_bar(acc), (uint32_t)((it >> 1) & 1) ^ 1u, args.wait_cycles, abort_flag)) {
                 ok = false;
                 break;
             }
             fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
             for (int kb = 0; kb < args.k_blocks; ++kb) {
-                if (*abort_flag || !mbar_wait(full_bar(stage), phase)) {
+                if (!mbar_wait_for(full_bar(stage), phase, args.wait_cycles, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -199,7 +200,8 @@ grouped_gemm_solo_kernel(const __grid_constant__ CUtensorMap tmA,
         int it = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
             const int acc = it & 1;
-            if (*abort_flag || !mbar_wait(tfull_bar(acc), (uint32_t)((it >> 1) & 1))) {
+            // the whole warp decides together (tcgen05.ld below is warp-wide)
+            if (!__all_sync(0xffffffffu, mbar_wait_for(tfull_bar(acc), (uint32_t)((it >> 1) & 1), args.wait_cycles, abort_flag))) {
                 *abort_flag = 1;
                 set_status(args.hdr, MOE_ERR_TIMEOUT);
                 break;
@@ -293,6 +295,7 @@ cudaError_t launch_gemm_solo_gate_up(const __nv_bfloat16* x_sorted, int64_t rows
     a.bn_out = 128;
     a.out = h;
     a.ld_out = I;
+    a.wait_cycles = main_wait_cycles();
     return launch_pdl(grouped_gemm_solo_kernel<true>, dim3(num_sms), dim3(256), SMEM_BYTES, s,
                       mA, mG, mU, a);
 }
@@ -316,6 +319,7 @@ cudaError_t launch_gemm_solo_down(const __nv_bfloat16* h, int64_t rows_alloc,
     a.bn_out = 256;
     a.out = y_sorted;
     a.ld_out = H;
+    a.wait_cycles = main_wait_cycles();
     return launch_pdl(grouped_gemm_solo_kernel<false>, dim3(num_sms), dim3(256), SMEM_BYTES, s,
                       mA, mD, mD, a);
 }

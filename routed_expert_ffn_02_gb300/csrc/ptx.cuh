@@ -22,7 +22,10 @@ __device__ __forceinline__ void grid_dep_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// A bounded wait gives up after this many SM cycles (~2 s at 2 GHz).
+// A bounded wait gives up after this many SM cycles (~2 s at 2 GHz).  The
+// main-loop waits of the expert kernels take their limit as a kernel
+// argument (this value unless a test shortened it); the waits that drain a
+// kernel's own copies and MMAs after an expiry always use this one.
 constexpr long long kWaitCycles = 4000000000LL;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -90,6 +93,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     return true;
 }
 
+// Same, giving up after `limit` cycles, or as soon as *abort is non-zero
+// (another role of the CTA gave up; abort may be null).
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, long long limit,
+                                              const volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long start = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if ((abort && *abort) || clock64() - start > limit) return false;
+    }
+    return true;
+}
+
+// Counts `bytes` of transactions on `bar` as complete without a copy (used
+// to close a phase whose bytes some copy will never deliver).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
 // Contiguous global -> shared copy on the bulk-copy (TMA) engine, completing
 // `bytes` transactions on `bar`.  dst, src 16-byte aligned; bytes % 16 == 0.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
@@ -137,6 +159,39 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// Shared -> global tensor store of one box at (x, y) in the bulk async-group
+// of the issuing thread; x * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            (uint64_t)map),
+        "r"(src), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until at most N of the thread's bulk groups still read their source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Waits until all of the thread's bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Orders this thread's shared-memory writes before later async-proxy reads
+// (a tensor store issued after a warp barrier).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
 // ---- thread-block clusters ----
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -153,6 +208,15 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
+}
+// 32-bit load / store at a shared::cluster address (any CTA of the cluster).
+__device__ __forceinline__ uint32_t ld_shared_cluster(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 // Arrive on a barrier given by its shared::cluster address (any CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {

@@ -136,17 +136,25 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 // ---- shared-memory layout and pipeline ------------------------------------
 
 // [slots x stage_bytes weight ring][activation buffer][barriers]
+// Each producer's copies into a slot complete on its own full barrier
+// (full(s) for producer 0, full2(s) for producer 1), so a producer that
+// stops early can still wait for exactly the copies it issued.
+constexpr int kBarriers = 3 * kMaxSlots + 2;
 struct Smem {
     uint32_t base;       // shared addresses
     uint32_t act;
     uint32_t bars;
     int stage_bytes;
     int slots;
+    int producers;
     __device__ uint32_t buf(int s) const { return base + (uint32_t)(s * stage_bytes); }
     __device__ uint32_t full(int s) const { return bars + 8u * s; }
     __device__ uint32_t empty(int s) const { return bars + 8u * (kMaxSlots + s); }
     __device__ uint32_t act_full() const { return bars + 8u * (2 * kMaxSlots); }
     __device__ uint32_t act_free() const { return bars + 8u * (2 * kMaxSlots + 1); }
+    __device__ uint32_t full2(int s) const { return bars + 8u * (2 * kMaxSlots + 2 + s); }
+    // full barrier of producer p
+    __device__ uint32_t full_of(int p, int s) const { return p == 0 ? full(s) : full2(s); }
 };
 
 __device__ __forceinline__ Smem smem_setup(uint8_t* smem, int stage_bytes, int slots,
@@ -155,11 +163,12 @@ __device__ __forceinline__ Smem smem_setup(uint8_t* smem, int stage_bytes, int s
     m.base = smem_u32(smem);
     m.stage_bytes = stage_bytes;
     m.slots = slots;
+    m.producers = producers;
     m.act = m.base + (uint32_t)(slots * stage_bytes);
     m.bars = m.act + (uint32_t)act_bytes;
     if (threadIdx.x == 0) {
         for (int s = 0; s < slots; ++s) {
-            mbar_init(m.full(s), producers);
+            for (int p = 0; p < producers; ++p) mbar_init(m.full_of(p, s), 1);
             mbar_init(m.empty(s), 1);
         }
         mbar_init(m.act_full(), 1);
@@ -212,10 +221,10 @@ __device__ __forceinline__ Range cta_range(const ThinUnit* units, int n_units, i
     return r;
 }
 
-// All lanes of a warp wait (bounded, convergent) for the phase with the given
-// parity.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
-    const bool ok = mbar_wait(bar, parity);
+// All lanes of a warp wait (bounded by `limit` cycles, convergent) for the
+// phase with the given parity.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, long long limit) {
+    const bool ok = mbar_wait_for(bar, parity, limit, nullptr);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -223,10 +232,12 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
 // (copy_item) and, if it is the `stager`, stages each unit's activations
 // (copy_act) once the consumers have released the previous unit's.  Items
 // [0, pre) (pre <= slots) were already issued into slots [0, pre).  While a
-// slot is still in use the lane sleeps in try_wait.  Returns false on a timeout.
+// slot is still in use the lane sleeps in try_wait.  Each wait gives up after
+// `limit` cycles; then the copies already issued are waited for (full bound)
+// and it returns false.
 template <typename ItemFn, typename ActFn>
-__device__ bool produce(const Smem& m, const Range& rg, bool stager, ItemFn copy_item,
-                        ActFn copy_act, int pre = 0) {
+__device__ bool produce(const Smem& m, int producer, const Range& rg, bool stager,
+                        ItemFn copy_item, ActFn copy_act, long long limit, int pre = 0) {
     if (rg.cnt <= 0) return true;
     int last_round[kMaxSlots];
     for (int s = 0; s < kMaxSlots; ++s) last_round[s] = s < pre ? 0 : -1;
@@ -251,14 +262,14 @@ __device__ bool produce(const Smem& m, const Range& rg, bool stager, ItemFn copy
             const long long start = clock64();
             while (!mbar_try_wait_sleep(m.empty(slot), par, 2000)) {
                 try_stage();
-                if (clock64() - start > kWaitCycles) {
+                if (clock64() - start > limit) {
                     ok = false;
                     break;
                 }
             }
             if (!ok) break;
         }
-        copy_item(rg.beg + seq, m.buf(slot), m.full(slot));
+        copy_item(rg.beg + seq, m.buf(slot), m.full_of(producer, slot));
         last_round[slot] = round;
         try_stage();
         if (++slot == m.slots) {
@@ -267,7 +278,7 @@ __device__ bool produce(const Smem& m, const Range& rg, bool stager, ItemFn copy
         }
     }
     while (ok && act_issued < n_units) {
-        if (!mbar_wait(m.act_free(), (uint32_t)((act_issued - 1) & 1))) {
+        if (!mbar_wait_for(m.act_free(), (uint32_t)((act_issued - 1) & 1), limit, nullptr)) {
             ok = false;
             break;
         }
@@ -277,7 +288,8 @@ __device__ bool produce(const Smem& m, const Range& rg, bool stager, ItemFn copy
     if (!ok) {
         // Let the copies already issued land before the CTA exits.
         for (int s = 0; s < m.slots; ++s)
-            if (last_round[s] >= 0) (void)mbar_wait(m.full(s), (uint32_t)(last_round[s] & 1));
+            if (last_round[s] >= 0)
+                (void)mbar_wait(m.full_of(producer, s), (uint32_t)(last_round[s] & 1));
         if (act_issued > 0) (void)mbar_wait(m.act_full(), (uint32_t)((act_issued - 1) & 1));
     }
     return ok;
@@ -323,13 +335,13 @@ __device__ __forceinline__ void with_slots(int n, F&& f) {
 // activations, then for the warp's items of that unit (seq = c mod nc) wait
 // for the slot and run item.template operator()<N>(item, slot) with N the
 // unit's slot count (the item releases the slot), then release the
-// activations.  Returns false on a timeout.
+// activations.  Returns false when a wait ran past `limit` cycles.
 template <int kExact, typename ItemFn>
 __device__ bool consume(const Smem& m, const Range& rg, int ipe, const ThinUnit* units, int c,
-                        int nc, ItemFn item) {
+                        int nc, long long limit, ItemFn item) {
     const int lane = threadIdx.x & 31;
     for (int u = rg.u_first; u <= rg.u_last; ++u) {
-        if (!warp_wait(m.act_full(), (uint32_t)((u - rg.u_first) & 1))) return false;
+        if (!warp_wait(m.act_full(), (uint32_t)((u - rg.u_first) & 1), limit)) return false;
         const int s0 = max(u * ipe, rg.beg) - rg.beg;
         const int s1 = min((u + 1) * ipe, rg.beg + rg.cnt) - rg.beg;
         const int first = s0 + ((c - s0 % nc) + nc) % nc;
@@ -337,11 +349,12 @@ __device__ bool consume(const Smem& m, const Range& rg, int ipe, const ThinUnit*
         with_slots<kExact>(units[u].n, [&]<int N>() {
             int slot = first % m.slots, round = first / m.slots;
             for (int seq = first; seq < s1; seq += nc) {
-                if (round > 0 && !warp_wait(m.empty(slot), (uint32_t)((round - 1) & 1))) {
+                if (round > 0 && !warp_wait(m.empty(slot), (uint32_t)((round - 1) & 1), limit)) {
                     ok = false;
                     return;
                 }
-                if (!warp_wait(m.full(slot), (uint32_t)(round & 1))) {
+                if (!warp_wait(m.full(slot), (uint32_t)(round & 1), limit) ||
+                    (m.producers > 1 && !warp_wait(m.full2(slot), (uint32_t)(round & 1), limit))) {
                     ok = false;
                     return;
                 }
@@ -609,7 +622,7 @@ thin_gate_up_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
                     const __nv_bfloat16* __restrict__ Wu, const ThinUnit* __restrict__ units,
                     const int32_t* __restrict__ wslot,
                     WsHeader* hdr, __nv_bfloat16* __restrict__ h, int stage_bytes, int slots,
-                    int act_bytes, SelfRoute sr) {
+                    int act_bytes, SelfRoute sr, long long wait_cycles) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ SmallPlan sp;
     constexpr int kProducers = 2;   // warp 0 issues the gate rows, warp 1 the up rows
@@ -645,7 +658,7 @@ thin_gate_up_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
             const __nv_bfloat16* W = warp == 0 ? Wg : Wu;
             const uint32_t part = warp == 0 ? 0u : half;
             const bool ok = produce(
-                m, rg, warp == 0,
+                m, warp, rg, warp == 0,
                 [&](int it, uint32_t dst, uint32_t bar) {
                     const ThinUnit un = U[it / ipe];
                     const size_t off =
@@ -658,13 +671,15 @@ thin_gate_up_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
                     mbar_expect_tx(bar, (uint32_t)un.n * xrow);
                     for (int t = 0; t < un.n; ++t)
                         bulk_g2s(dst + t * xrow, x + (size_t)(order[un.row0 + t] / k) * H, xrow, bar);
-                });
+                },
+                wait_cycles);
             if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
         }
         return;
     }
 
-    const bool ok = consume<16>(m, rg, ipe, U, warp - kProducers, nc, [&]<int N>(int it, int slot) {
+    const bool ok = consume<16>(m, rg, ipe, U, warp - kProducers, nc, wait_cycles,
+                                [&]<int N>(int it, int slot) {
         const ThinUnit un = U[it / ipe];
         __nv_bfloat16* hcol = h + (int64_t)un.row0 * I + (it % ipe) * R;
         gate_up_slot<N, VPL>(m, slot, R, vec, un.n, hcol, I);
@@ -680,7 +695,7 @@ thin_down_kernel(const __nv_bfloat16* __restrict__ h, int H, int I, int R,
                  const __nv_bfloat16* __restrict__ Wd, const ThinUnit* __restrict__ units,
                  const int32_t* __restrict__ wslot, WsHeader* hdr,
                  __nv_bfloat16* __restrict__ y, int stage_bytes, int slots, int act_bytes,
-                 SelfRoute sr) {
+                 SelfRoute sr, long long wait_cycles) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ SmallPlan sp;
     constexpr int kProducers = 1;
@@ -727,14 +742,14 @@ thin_down_kernel(const __nv_bfloat16* __restrict__ h, int H, int I, int R,
             grid_dep_wait();
             grid_dep_launch();
             const bool ok = produce(
-                m, rg, true, copy_item,
+                m, 0, rg, true, copy_item,
                 [&](int u, uint32_t dst, uint32_t bar) {
                     const ThinUnit un = U[u];
                     // the unit's h rows are consecutive sorted positions
                     mbar_expect_tx(bar, (uint32_t)un.n * hrow);
                     bulk_g2s(dst, h + (size_t)un.row0 * I, (uint32_t)un.n * hrow, bar);
                 },
-                pre);
+                wait_cycles, pre);
             if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
         }
     } else {
@@ -742,7 +757,7 @@ thin_down_kernel(const __nv_bfloat16* __restrict__ h, int H, int I, int R,
         grid_dep_launch();
         constexpr int kExact =
             (VPL > 0 && DownRegSlots<VPL>::value > 0) ? DownRegSlots<VPL>::value : 16;
-        const bool ok = consume<kExact>(m, rg, ipe, U, warp - kProducers, nc,
+        const bool ok = consume<kExact>(m, rg, ipe, U, warp - kProducers, nc, wait_cycles,
                                         [&]<int N>(int it, int slot) {
             const ThinUnit un = U[it / ipe];
             __nv_bfloat16* ycol = y + (int64_t)un.row0 * H + (it % ipe) * R;
@@ -780,7 +795,7 @@ Geometry geometry(int row_bytes, int act_row_bytes, int act_tokens, bool pad4) {
     g.slots = (kSmemBudget - g.act) / g.stage;
     if (g.slots > kMaxSlots) g.slots = kMaxSlots;
     if (g.slots < 2) g.slots = 2;
-    g.smem = g.slots * g.stage + g.act + 8 * (2 * kMaxSlots + 2);
+    g.smem = g.slots * g.stage + g.act + 8 * kBarriers;
     return g;
 }
 
@@ -802,7 +817,7 @@ cudaError_t launch_gu(const __nv_bfloat16* x, const int32_t* perm, int k, int H,
     if (e != cudaSuccess) return e;
     return launch_pdl(thin_gate_up_kernel<V>, dim3(num_sms), dim3(threads_for(g, 2)), g.smem, s,
                       x, perm, k, H, I, g.R, Wg, Wu, plan.units, plan.wslot, plan.hdr, h, g.stage,
-                      g.slots, g.act, sr);
+                      g.slots, g.act, sr, main_wait_cycles());
 }
 
 template <int V>
@@ -814,7 +829,7 @@ cudaError_t launch_d(const __nv_bfloat16* h, int H, int I, const __nv_bfloat16* 
     if (e != cudaSuccess) return e;
     return launch_pdl(thin_down_kernel<V>, dim3(num_sms), dim3(threads_for(g, 1)), g.smem, s, h,
                       H, I, g.R, Wd, plan.units, plan.wslot, plan.hdr, y, g.stage, g.slots, g.act,
-                      sr);
+                      sr, main_wait_cycles());
 }
 
 }  // namespace

@@ -74,6 +74,7 @@ struct ThinMmaArgs {
     __nv_bfloat16* out;       // [rows_alloc, ld_out]
     int64_t ld_out;
     SelfRoute sr;             // logits != nullptr: the batch routes itself
+    long long wait_cycles;     // limit of each main-loop wait (SM cycles)
 };
 
 template <bool kGated>
@@ -164,7 +165,7 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
             const int wrow = weight_block(args.wslot, ft.expert) * args.w_rows_per_expert +
                              (t % args.n_blocks) * BM;
             for (int kb = 0; kb < args.k_blocks; ++kb) {
-                if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
+                if (!mbar_wait_for(empty_bar(stage), phase ^ 1u, args.wait_cycles, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -203,14 +204,14 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
         bool issued = false;
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++it) {
             const int acc = it & 1;
-            if (*abort_flag || !mbar_wait(tempty_bar(acc), (uint32_t)((it >> 1) & 1) ^ 1u)) {
+            if (!mbar_wait_for(tempty_bar(acc), (uint32_t)((it >> 1) & 1) ^ 1u, args.wait_cycles, abort_flag)) {
                 ok = false;
                 break;
             }
             fence_after();
             const uint32_t d0 = tmem_base + (uint32_t)(acc * C::kAccCols);
             for (int kb = 0; kb < args.k_blocks; ++kb) {
-                if (*abort_flag || !mbar_wait(full_bar(stage), phase)) {
+                if (!mbar_wait_for(full_bar(stage), phase, args.wait_cycles, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -254,7 +255,8 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
             const FatTile ft = ft_next;
             if (t + (int)gridDim.x < total) ft_next = tile_at((t + gridDim.x) / args.n_blocks);
             const int acc = it & 1;
-            if (*abort_flag || !mbar_wait(tfull_bar(acc), (uint32_t)((it >> 1) & 1))) {
+            // the whole warp decides together (tcgen05.ld below is warp-wide)
+            if (!__all_sync(0xffffffffu, mbar_wait_for(tfull_bar(acc), (uint32_t)((it >> 1) & 1), args.wait_cycles, abort_flag))) {
                 *abort_flag = 1;
                 set_status(args.hdr, MOE_ERR_TIMEOUT);
                 break;
@@ -327,6 +329,7 @@ cudaError_t launch_thin_mma_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_
     a.w_rows_per_expert = I;
     a.out = h;
     a.ld_out = I;
+    a.wait_cycles = main_wait_cycles();
     a.sr = sr ? *sr : SelfRoute{};
     return launch_pdl(thin_mma_kernel<true>, dim3(num_sms), dim3(256), Cfg<true>::kSmemBytes, s,
                       mX, mG, mU, mXr, a);
@@ -351,6 +354,7 @@ cudaError_t launch_thin_mma_down(const __nv_bfloat16* h, int64_t rows_alloc,
     a.w_rows_per_expert = H;
     a.out = y_sorted;
     a.ld_out = H;
+    a.wait_cycles = main_wait_cycles();
     a.sr = sr ? *sr : SelfRoute{};
     return launch_pdl(thin_mma_kernel<false>, dim3(num_sms), dim3(256), Cfg<false>::kSmemBytes, s,
                       mX, mD, mD, mX, a);
