@@ -137,8 +137,8 @@ def test_stager_argument_errors(moe):
 def test_forward_launch_count(moe):
     """Kernels one moe_forward launches: route, route lists (1 or 3), then
     only the expert kernels that can have work, then combine.  Small batches
-    on the CUDA-core streaming kernels route inside them and combine in the
-    down kernel: gate/up, down."""
+    on one streaming kernel route inside it and combine in the down kernel:
+    gate/up, down."""
     S = moe.Shape
     # decode: 8 or 16 touched experts x 16 blocks < 384 items -> CUDA cores,
     # from 24 x 16 = 384 on tensor cores; up to 32 slots the batch is routed
@@ -150,8 +150,12 @@ def test_forward_launch_count(moe):
     assert moe.forward_launches(S(1, 384, 8, 4096, 2048, thin_mma_min=1)) == 2
     assert moe.forward_launches(S(4, 384, 8, 4096, 2048, thin_mma_min=33)) == 2
     assert moe.forward_launches(S(4, 384, 8, 4096, 2048, thin_mma_min=3)) == 8   # split kernels
-    assert moe.forward_launches(S(8, 384, 8, 4096, 2048)) == 6       # 64 slots: planned
-    # self-routing limits: 32 slots, below the fat threshold, one unit per expert
+    for B in (5, 8, 16, 24):                                 # decode sweep: > 32 slots
+        assert moe.forward_launches(S(B, 384, 8, 4096, 2048)) == 6
+    assert moe.forward_launches(S(32, 64, 8, 512, 256, 33, 1)) == 6   # 256 slots
+    assert moe.forward_launches(S(32, 64, 8, 512, 256, 32, 1)) == 10  # T = 32 may be fat
+    # CUDA-core self-routing limits: 32 slots, below the fat threshold, one
+    # unit per expert
     assert moe.forward_launches(S(5, 384, 8, 4096, 2048, thin_mma_min=33)) == 5   # 40 slots
     assert moe.forward_launches(S(32, 64, 1, 512, 256, thin_mma_min=33)) == 10    # T = 32 may be fat
     assert moe.forward_launches(S(16, 64, 2, 512, 256, thin_mma_min=33)) == 2     # unit of 16

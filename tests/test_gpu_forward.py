@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import synth
-from parity import DeviceExperts, GATE_ATOL, assert_close, oracle_rows
+from parity import DeviceExperts, GATE_ATOL, assert_close, oracle_rows, sample_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -294,6 +294,60 @@ def big_layer():
     yield dict(Wg=Wg, Wu=Wu, Wd=Wd)
     del Wg, Wu, Wd
     torch.cuda.empty_cache()
+
+
+def _forward_vs_entry_points(moe, s, shape, d, inp, launches):
+    """moe_forward on a whole batch: the expected launch count, routing
+    bit-exact, every output against the oracle, and bit-identical to router,
+    route lists, expert FFN and combine called one by one."""
+    assert moe.forward_launches(shape) == launches
+    out, idx, gates = _forward(moe, shape, d)
+    experts = DeviceExperts(d["Wg"], d["Wu"], d["Wd"])
+    ref, ridx, rgates = oracle_rows(synth.bf16_bits(inp["x"]), inp["logits"].numpy(), s.k,
+                                    experts, np.arange(s.T))
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    assert np.allclose(gates.cpu().numpy(), rgates, rtol=0, atol=GATE_ATOL)
+    assert_close(out, ref, f"self-routed {s}")
+    idx2, gates2 = moe.moe_route(d["logits"], s.k)
+    counts, offsets, perm, inv = moe.moe_permute(idx2, s.E)
+    y = moe.moe_expert_ffn(shape, d["x"], perm, offsets, counts, d["Wg"], d["Wu"], d["Wd"])
+    out2 = moe.moe_combine(y, inv, gates2, s.T, s.k, s.H)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx2) and torch.equal(gates, gates2)
+    assert torch.equal(out, out2)
+
+
+# Batches of 33..256 slots on the tensor-core streaming kernel run the
+# router, route-list, gather and combine kernels (measured faster than routing
+# inside the streaming kernels at these sizes): six launches.
+PLANNED_MMA = [
+    # T, E, k, H, I, fat threshold
+    (12, 5, 3, 768, 512, 32),      # 36 slots on 5 experts (up to 12 slots each)
+    (20, 1024, 8, 256, 256, 32),   # 160 slots, E = 1024
+    (32, 64, 8, 512, 256, 33),     # 256 slots: the plan's capacity
+    (9, 40, 6, 1280, 768, 32),     # 54 slots, k = 6, H not a power of two
+]
+
+
+@pytest.mark.parametrize("T,E,k,H,I,thr", PLANNED_MMA)
+def test_forward_mma_batches_33_to_256_slots(moe, T, E, k, H, I, thr):
+    s = synth.Shape(T=T, E=E, k=k, H=H, I=I)
+    inp = synth.make_layer(s, seed=300 + T, zipf_s=synth.ZIPF_S)
+    shape = moe.Shape(T, E, k, H, I, fat_threshold=thr, thin_mma_min=MMA_ALL)
+    _forward_vs_entry_points(moe, s, shape, _to_dev(inp), inp, 6)
+
+
+@pytest.mark.parametrize("B", [5, 8, 16, 24])
+def test_forward_decode_sweep_batches(moe, big_layer, B):
+    """Decode batches 5..24 at full size (E=384, top-8, H=4096, I=2048), the
+    decode sweep's batches, on the tensor-core streaming kernels (the default
+    for these shapes), every output against the oracle."""
+    s = synth.Shape(T=B, E=384, k=8, H=4096, I=2048)
+    inp = dict(x=synth.make_x(B, s.H, seed=400 + B),
+               logits=synth.make_logits(B, s.E, seed=400 + B, zipf_s=synth.ZIPF_S))
+    d = dict(_to_dev(inp), **big_layer)
+    shape = moe.Shape(B, s.E, s.k, s.H, s.I)
+    _forward_vs_entry_points(moe, s, shape, d, inp, 6)
 
 
 @pytest.mark.parametrize("mma_min", [MMA_ALL, MMA_NONE])
