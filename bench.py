@@ -840,15 +840,16 @@ def run_gpu(args):
 
 
 def run_decode_profile(args):
-    """A few eager decode forwards at batch B on the full E=384, H=4096,
-    I=2048 layer, 8 logit sets rotated (so each forward touches new
-    experts); prints mean stage times.  For ncu."""
+    """A few eager decode forwards at batch B on a layer of E experts (384 by
+    default, --experts to shrink it for profilers), H=4096, I=2048, 8 logit
+    sets rotated (so each forward touches new experts); prints mean stage
+    times.  For ncu."""
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     import routed_expert_ffn_02_gb300 as moe
     B = args.decode_profile
-    shape = moe.Shape(B, PREFILL.E, PREFILL.k, PREFILL.H, PREFILL.I, FAT_THRESHOLD,
-                      args.thin_mma_min)
+    shape = moe.Shape(B, args.experts or PREFILL.E, PREFILL.k, PREFILL.H, PREFILL.I,
+                      FAT_THRESHOLD, args.thin_mma_min)
     layer = Layer(moe, shape, dev, n_logit_sets=8)
     _, stage_ms = time_steps(layer, 8, 3)
     print(json.dumps({"decode_profile": f"B{B}",
