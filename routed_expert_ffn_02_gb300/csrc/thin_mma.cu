@@ -137,7 +137,14 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
         }
     }
     const int n_tiles = self ? sp.n_units : args.hdr_ro->n_thin_mma;
-    const int total = n_tiles * args.n_blocks;   // CTAs past it idle
+    const int total = n_tiles * args.n_blocks;
+    // Items go round-robin to the first `active` CTAs, as many as keep every
+    // wave full: one SM streams well below its share of HBM bandwidth when
+    // few others run, so a last wave of a few items (8 of 616 at decode batch
+    // 24) would run alone at that rate.  The other CTAs take no item.
+    const int waves = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int active = waves > 0 ? (total + waves - 1) / waves : 1;
+    const int first = (int)blockIdx.x < active ? (int)blockIdx.x : total;
     auto tile_at = [&](int i) {
         if (!self) return args.tiles[i];
         const ThinUnit u = sp.units[i];
@@ -158,10 +165,10 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
         bool ok = true;
         // Each item's tile is loaded one item ahead (its latency is hidden).
         FatTile ft_next = {};
-        if ((int)blockIdx.x < total) ft_next = tile_at(blockIdx.x / args.n_blocks);
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        if (first < total) ft_next = tile_at(first / args.n_blocks);
+        for (int t = first; ok && t < total; t += active) {
             const FatTile ft = ft_next;
-            if (t + (int)gridDim.x < total) ft_next = tile_at((t + gridDim.x) / args.n_blocks);
+            if (t + active < total) ft_next = tile_at((t + active) / args.n_blocks);
             const int wrow = weight_block(args.wslot, ft.expert) * args.w_rows_per_expert +
                              (t % args.n_blocks) * BM;
             for (int kb = 0; kb < args.k_blocks; ++kb) {
@@ -202,7 +209,7 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
         int it = 0;
         bool ok = true;
         bool issued = false;
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++it) {
+        for (int t = first; ok && t < total; t += active, ++it) {
             const int acc = it & 1;
             if (!mbar_wait_for(tempty_bar(acc), (uint32_t)((it >> 1) & 1) ^ 1u, args.wait_cycles, abort_flag)) {
                 ok = false;
@@ -250,10 +257,10 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
         const int ew = warp - 4;   // TMEM lanes (weight rows) 32*ew .. 32*ew+31
         int it = 0;
         FatTile ft_next = {};
-        if ((int)blockIdx.x < total) ft_next = tile_at(blockIdx.x / args.n_blocks);
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+        if (first < total) ft_next = tile_at(first / args.n_blocks);
+        for (int t = first; t < total; t += active, ++it) {
             const FatTile ft = ft_next;
-            if (t + (int)gridDim.x < total) ft_next = tile_at((t + gridDim.x) / args.n_blocks);
+            if (t + active < total) ft_next = tile_at((t + active) / args.n_blocks);
             const int acc = it & 1;
             // the whole warp decides together (tcgen05.ld below is warp-wide)
             if (!__all_sync(0xffffffffu, mbar_wait_for(tfull_bar(acc), (uint32_t)((it >> 1) & 1), args.wait_cycles, abort_flag))) {
