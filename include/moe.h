@@ -193,9 +193,13 @@ size_t moe_workspace_size(const moe_shape* shape);
  * out [T, H] bf16 written.  topk_idx [T, k] / gates [T, k] may be NULL; when
  * given they receive the routing.  ws: moe_workspace_size() bytes,
  * initialised once with moe_workspace_init().  Batches of at most 32 token
- * slots whose experts all stream on the CUDA-core kernel (decode) run as two
- * kernels that route and combine inside themselves; the results, topk_idx
- * and gates included, are bit-identical to the separate stages. */
+ * slots whose experts all stream on one weight-streaming kernel (decode) run
+ * as two kernels that route and combine inside themselves, or, on the
+ * CUDA-core kernel at H = 4096, I = 2048 and H = 512, I = 256, as one
+ * cooperative kernel (one CTA per SM) that also waits, bounded, between its
+ * gate/up and down phases for every CTA; the results, topk_idx and gates
+ * included, are bit-identical to the separate stages.  Calls that share a
+ * workspace must be ordered on one stream (or otherwise serialised). */
 moe_status moe_forward(const moe_shape* shape, const float* logits,
                        const moe_bf16* x, const moe_bf16* W_gate,
                        const moe_bf16* W_up, const moe_bf16* W_down,
@@ -214,7 +218,8 @@ moe_status moe_forward(const moe_shape* shape, const float* logits,
  *   [7] after the thin down  [8] after the combine
  * A stage with nothing to do still records its event (for the two-kernel
  * small batches, routing and route lists are inside the thin gate/up stage
- * and the combine inside the thin down stage).  stage_events must
+ * and the combine inside the thin down stage; the one-kernel layer is all
+ * inside the thin gate/up stage).  stage_events must
  * hold n_events >= MOE_PROFILE_EVENTS entries; a NULL entry is skipped.
  * Results are identical to moe_forward. */
 moe_status moe_forward_profiled(const moe_shape* shape, const float* logits,
@@ -225,7 +230,8 @@ moe_status moe_forward_profiled(const moe_shape* shape, const float* logits,
                                 void* const* stage_events, int32_t n_events);
 
 /* Number of kernels one moe_forward call with this shape launches (the
- * launch sequence depends only on the shape; 2 for the small batches above),
+ * launch sequence depends only on the shape; 1 or 2 for the small batches
+ * above),
  * or -1 for an invalid shape. */
 int32_t moe_forward_launches(const moe_shape* shape);
 

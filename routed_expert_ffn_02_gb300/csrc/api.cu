@@ -309,7 +309,16 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
                  "grouped GEMM gate/up (solo tiles)");
     }
     CUDA_TRY(mark(ev, kEvGemmGateUp, s), "cudaEventRecord");
-    {
+    // A self-routed batch on the CUDA-core streaming kernel alone runs the
+    // whole layer in one cooperative launch where that kernel has a build for
+    // the layer's width (its stage events then bracket it as gate/up).
+    const bool one_launch = sr && kn.units && !kn.mma && !kn.fat && thin_layer_fused(H, I);
+    if (one_launch) {
+        const Nvtx r("moe.thin_layer");
+        CUDA_TRY(launch_thin_layer(x, sh->k, H, I, Wg, Wu, Wd, plan, fat_bound, h, y, sms, s,
+                                   *sr),
+                 "thin layer");
+    } else {
         const Nvtx r("moe.thin_gate_up");
         if (kn.units)
             CUDA_TRY(launch_thin_gate_up(x, perm, sh->k, H, I, Wg, Wu, plan, fat_bound, h, sms, s,
@@ -329,7 +338,7 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
     CUDA_TRY(mark(ev, kEvGemmDown, s), "cudaEventRecord");
     {
         const Nvtx r("moe.thin_down");
-        if (kn.units)
+        if (kn.units && !one_launch)
             CUDA_TRY(launch_thin_down(h, H, I, Wd, plan, fat_bound, y, sms, s, sr), "thin down");
         if (kn.mma)
             CUDA_TRY(launch_thin_mma_down(h, ra, Wd, H, I, plan, y, sms, s, sr),
@@ -552,7 +561,9 @@ moe_status moe_forward_profiled(const moe_shape* shape, const float* logits,
 int32_t moe_forward_launches(const moe_shape* shape) {
     if (check_shape(shape) != MOE_OK) return -1;
     if (shape->T == 0) return 0;
-    if (self_mode(shape) != kPlanned) return 2;      // gate/up, down (routing, combine inside)
+    const SelfMode sm = self_mode(shape);
+    if (sm == kSelfUnits && thin_layer_fused(shape->H, shape->I)) return 1;   // the whole layer
+    if (sm != kPlanned) return 2;                    // gate/up, down (routing, combine inside)
     const int64_t P = (int64_t)shape->T * shape->k;
     int32_t n = 1;                                   // route
     n += (P <= kPermChunk) ? 1 : 3;                  // route lists (+ planner)

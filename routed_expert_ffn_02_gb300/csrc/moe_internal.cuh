@@ -30,7 +30,9 @@ struct WsHeader {
     int32_t n_thin_mma;    // thin experts on the tensor-core streaming kernel
     int32_t n_solo;        // fat experts' leftover 128-row tiles (one-CTA GEMM)
     int32_t ticket;        // CTAs of a streaming down kernel done (fused combine)
-    int32_t reserved[57];
+    uint32_t layer_sync;   // CTAs past the gate/up phase of the one-kernel decode layer
+                           // (monotonic: a launch waits for its own multiple of the grid)
+    int32_t reserved[56];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -221,6 +223,18 @@ cudaError_t launch_thin_gate_up(const __nv_bfloat16* x, const int32_t* perm, int
 cudaError_t launch_thin_down(const __nv_bfloat16* h, int H, int I, const __nv_bfloat16* Wd,
                              const Plan& plan, int64_t max_slots, __nv_bfloat16* y_sorted,
                              int num_sms, cudaStream_t s, const SelfRoute* sr = nullptr);
+
+// A self-routed batch on the CUDA-core streaming path as one cooperative
+// kernel: gate/up, a grid-wide wait (bounded) until every CTA's h rows are
+// stored, down (its first weight rows copied before that wait), and the
+// last CTA's combine.  thin_layer_fused(H, I) says whether it is built for
+// those sizes; otherwise the two kernels above run.
+bool thin_layer_fused(int H, int I);
+cudaError_t launch_thin_layer(const __nv_bfloat16* x, int k, int H, int I,
+                              const __nv_bfloat16* Wg, const __nv_bfloat16* Wu,
+                              const __nv_bfloat16* Wd, const Plan& plan, int64_t max_slots,
+                              __nv_bfloat16* h, __nv_bfloat16* y_sorted, int num_sms,
+                              cudaStream_t s, const SelfRoute& sr);
 
 // Weight streaming on tcgen05 for the thin experts in plan.mma_tiles:
 // gate_up: h[rows] = silu(x_sorted[rows] Wg_e^T) * (x_sorted[rows] Wu_e^T);

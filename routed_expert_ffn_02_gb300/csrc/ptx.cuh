@@ -105,6 +105,25 @@ __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, lon
     return true;
 }
 
+// Invalidates a barrier so its shared memory can be used again (for another
+// barrier or data); no thread may be waiting on it.
+__device__ __forceinline__ void mbar_inval(uint32_t bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// GPU-scope acquire load of a counter in global memory.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Orders this thread's global-memory accesses by ordinary loads and stores
+// with later accesses by the copy engine (bulk and tensor copies), either way.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Counts `bytes` of transactions on `bar` as complete without a copy (used
 // to close a phase whose bytes some copy will never deliver).
 __device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {

@@ -138,17 +138,19 @@ def test_forward_launch_count(moe):
     """Kernels one moe_forward launches: route, route lists (1 or 3), then
     only the expert kernels that can have work, then combine.  Small batches
     on one streaming kernel route inside it and combine in the down kernel:
-    gate/up, down."""
+    gate/up, down; on the CUDA-core kernel at H=4096, I=2048 or H=512,
+    I=256, one cooperative launch for the whole layer."""
     S = moe.Shape
     # decode: 8 or 16 touched experts x 16 blocks < 384 items -> CUDA cores,
     # from 24 x 16 = 384 on tensor cores; up to 32 slots the batch is routed
     # inside the streaming kernels either way
-    assert moe.forward_launches(S(1, 384, 8, 4096, 2048)) == 2
-    assert moe.forward_launches(S(2, 384, 8, 4096, 2048)) == 2
+    assert moe.forward_launches(S(1, 384, 8, 4096, 2048)) == 1
+    assert moe.forward_launches(S(2, 384, 8, 4096, 2048)) == 1
     assert moe.forward_launches(S(3, 384, 8, 4096, 2048)) == 2
     assert moe.forward_launches(S(4, 384, 8, 4096, 2048)) == 2
     assert moe.forward_launches(S(1, 384, 8, 4096, 2048, thin_mma_min=1)) == 2
-    assert moe.forward_launches(S(4, 384, 8, 4096, 2048, thin_mma_min=33)) == 2
+    assert moe.forward_launches(S(4, 384, 8, 4096, 2048, thin_mma_min=33)) == 1
+    assert moe.forward_launches(S(2, 384, 8, 2048, 1024)) == 2    # no one-launch build
     assert moe.forward_launches(S(4, 384, 8, 4096, 2048, thin_mma_min=3)) == 8   # split kernels
     for B in (5, 8, 16, 24):                                 # decode sweep: > 32 slots
         assert moe.forward_launches(S(B, 384, 8, 4096, 2048)) == 6
@@ -158,7 +160,7 @@ def test_forward_launch_count(moe):
     # unit per expert
     assert moe.forward_launches(S(5, 384, 8, 4096, 2048, thin_mma_min=33)) == 5   # 40 slots
     assert moe.forward_launches(S(32, 64, 1, 512, 256, thin_mma_min=33)) == 10    # T = 32 may be fat
-    assert moe.forward_launches(S(16, 64, 2, 512, 256, thin_mma_min=33)) == 2     # unit of 16
+    assert moe.forward_launches(S(16, 64, 2, 512, 256, thin_mma_min=33)) == 1     # unit of 16
     assert moe.forward_launches(S(13, 64, 2, 4096, 2048, thin_mma_min=33)) == 5   # units of 12
     assert moe.forward_launches(S(2, 64, 2, 512, 256, fat_threshold=0)) == 8     # every expert fat
     # fat experts: pair GEMMs and solo-tile GEMMs for gate/up and down

@@ -47,6 +47,13 @@ def _forward(moe, shape, d, profiled=False):
 # thin_mma_min values: 1 = every thin expert on the tensor-core streaming
 # kernel, 33 = every thin expert on the CUDA-core one (0 = chosen by shape).
 MMA_ALL, MMA_NONE = 1, 33
+# Widths at which a self-routed batch on the CUDA-core streaming kernel runs
+# the whole layer in one cooperative launch (two launches elsewhere).
+ONE_LAUNCH_WIDTHS = {(4096, 2048), (512, 256)}
+
+
+def self_routed_launches(H, I, mma_min):
+    return 1 if mma_min == MMA_NONE and (H, I) in ONE_LAUNCH_WIDTHS else 2
 
 
 def _full_check(moe, s, thr, inp, d=None, mma_min=0):
@@ -144,7 +151,8 @@ def test_forward_threshold_edges(moe, mma_min):
 
 
 # Small batches route themselves inside the streaming kernels and combine in
-# the down kernel (two launches): T*k <= 32, T below the fat threshold, all
+# the down kernel (two launches, or one at the one-launch widths on the
+# CUDA-core kernel): T*k <= 32, T below the fat threshold, all
 # touched experts on the tensor-core kernel or all on the CUDA-core kernel
 # within one streaming unit.
 SELF_ROUTED = [
@@ -169,7 +177,7 @@ def test_forward_self_routed(moe, T, E, k, H, I, mma_min):
     inp = synth.make_layer(s, seed=100 + T, zipf_s=synth.ZIPF_S)
     d = _to_dev(inp)
     shape = moe.Shape(T, E, k, H, I, fat_threshold=32, thin_mma_min=mma_min)
-    assert moe.forward_launches(shape) == 2
+    assert moe.forward_launches(shape) == self_routed_launches(H, I, mma_min)
     _full_check(moe, s, 32, inp, d, mma_min=mma_min)
     out, idx, gates = _forward(moe, shape, d)
     idx2, gates2 = moe.moe_route(d["logits"], k)
@@ -213,21 +221,25 @@ def test_forward_self_routed_ties_and_reuse(moe):
     assert_close(out, ref, "self-routed ties")
 
 
-@pytest.mark.parametrize("mma_min", [MMA_NONE, MMA_ALL])
-def test_forward_self_routed_back_to_back(moe, mma_min):
+@pytest.mark.parametrize("H,I,mma_min", [(1024, 512, MMA_NONE), (1024, 512, MMA_ALL),
+                                         (512, 256, MMA_NONE)])
+def test_forward_self_routed_back_to_back(moe, H, I, mma_min):
     """Self-routed decode steps of batch 1, 2 and 4 enqueued back to back on
     one workspace with no synchronisation between them (programmatic
     dependent launch on): every step's fused combine counts its down CTAs on
     the same ticket word, so a ticket left behind by one step would make the
-    next step combine early or not at all.  Each step against the oracle."""
-    E, k, H, I = 64, 8, 1024, 512
+    next step combine early or not at all; the one-launch layer (H=512,
+    I=256) also counts its CTAs between the gate/up and down phases on one
+    word, which a step must leave at a multiple of the grid.  Each step
+    against the oracle."""
+    E, k = 64, 8
     Wg, Wu, Wd = synth.make_weights(E, H, I, seed=21, layer=0, device="cuda")
     experts = DeviceExperts(Wg, Wu, Wd)
     batches = [1, 2, 4, 4, 1, 2, 1, 4]
     shapes = {B: moe.Shape(B, E, k, H, I, fat_threshold=32, thin_mma_min=mma_min)
               for B in set(batches)}
     for sh in shapes.values():
-        assert moe.forward_launches(sh) == 2
+        assert moe.forward_launches(sh) == self_routed_launches(H, I, mma_min)
     ws = moe.Workspace(max(moe.workspace_size(sh) for sh in shapes.values()))
     steps = []
     for r, B in enumerate(batches):
@@ -348,6 +360,20 @@ def test_forward_decode_sweep_batches(moe, big_layer, B):
     d = dict(_to_dev(inp), **big_layer)
     shape = moe.Shape(B, s.E, s.k, s.H, s.I)
     _forward_vs_entry_points(moe, s, shape, d, inp, 6)
+
+
+@pytest.mark.parametrize("B,mma_min", [(1, 0), (2, 0), (4, MMA_NONE)])
+def test_forward_decode_one_launch(moe, big_layer, B, mma_min):
+    """Full-size decode batches on the CUDA-core streaming kernel (batches 1
+    and 2 by default, 4 when forced: 32 slots): the whole layer in one
+    cooperative launch, every output against the oracle and bit-identical to
+    the separate entry points."""
+    s = synth.Shape(T=B, E=384, k=8, H=4096, I=2048)
+    inp = dict(x=synth.make_x(B, s.H, seed=500 + B),
+               logits=synth.make_logits(B, s.E, seed=500 + B, zipf_s=synth.ZIPF_S))
+    d = dict(_to_dev(inp), **big_layer)
+    shape = moe.Shape(B, s.E, s.k, s.H, s.I, thin_mma_min=mma_min)
+    _forward_vs_entry_points(moe, s, shape, d, inp, 1)
 
 
 @pytest.mark.parametrize("mma_min", [MMA_ALL, MMA_NONE])

@@ -72,15 +72,20 @@ def test_expert_kernel_wait_expiry(moe, case):
         assert torch.equal(after, before), case
 
 
-@pytest.mark.parametrize("mma_min", [MMA_NONE, MMA_ALL])
-def test_self_routed_decode_wait_expiry(moe, mma_min):
+@pytest.mark.parametrize("H,I,mma_min,launches", [(1024, 512, MMA_NONE, 2),
+                                                  (1024, 512, MMA_ALL, 2),
+                                                  (512, 256, MMA_NONE, 1)])
+def test_self_routed_decode_wait_expiry(moe, H, I, mma_min, launches):
     """A decode step routed inside the streaming kernels (two launches, the
-    combine fused into the down kernel) that times out, then normal steps on
-    the same workspace: status MOE_ERR_TIMEOUT once, then correct outputs."""
-    B, E, k, H, I = 2, 64, 8, 1024, 512
+    combine fused into the down kernel; or, at H=512, I=256 on CUDA cores,
+    the whole layer in one cooperative launch whose down phase also waits,
+    bounded, for every CTA's gate/up phase) that times out, then normal steps
+    on the same workspace: status MOE_ERR_TIMEOUT once, then correct
+    outputs."""
+    B, E, k = 2, 64, 8
     Wg, Wu, Wd = synth.make_weights(E, H, I, seed=41, layer=0, device="cuda")
     shape = moe.Shape(B, E, k, H, I, fat_threshold=32, thin_mma_min=mma_min)
-    assert moe.forward_launches(shape) == 2
+    assert moe.forward_launches(shape) == launches
     ws = moe.Workspace(moe.workspace_size(shape))
     x = synth.make_x(B, H, seed=41)
     lg = synth.make_logits(B, E, seed=41, zipf_s=synth.ZIPF_S)
@@ -90,10 +95,11 @@ def test_self_routed_decode_wait_expiry(moe, mma_min):
     assert ws.status() == 0
     _timed_out(moe, lambda: moe.moe_forward(shape, lgd, xd, Wg, Wu, Wd, ws=ws))
     assert ws.status(clear=True) == MOE_ERR_TIMEOUT
-    after = moe.moe_forward(shape, lgd, xd, Wg, Wu, Wd, ws=ws)
-    torch.cuda.synchronize()
-    assert ws.status() == 0
-    assert torch.equal(after, before)
+    for _ in range(2):
+        after = moe.moe_forward(shape, lgd, xd, Wg, Wu, Wd, ws=ws)
+        torch.cuda.synchronize()
+        assert ws.status() == 0
+        assert torch.equal(after, before)
     ref, _, _ = oracle_rows(synth.bf16_bits(x), lg.numpy(), k, DeviceExperts(Wg, Wu, Wd),
                             np.arange(B))
     assert_close(after, ref, "decode after a timed-out step")
