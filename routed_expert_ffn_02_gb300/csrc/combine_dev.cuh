@@ -10,18 +10,16 @@
 
 namespace moe {
 
-// load(i): 16-byte vector i of y_sorted; src[j]: first vector of slot j's row.
-template <typename Load>
-__device__ __forceinline__ uint4 combine_vec(Load load, const int64_t (&src)[kMaxK],
-                                             const float (&g)[kMaxK], int k, int64_t v) {
+// r[j]: the 16-byte vector of slot j's y row (j < k); g[j]: its gate.
+__device__ __forceinline__ uint4 combine_vals(const uint4 (&r)[kMaxK], const float (&g)[kMaxK],
+                                              int k) {
     float acc[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
         if (j < k) {
-            const uint4 r = load(src[j] + v);
-            const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&r);
+            const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&r[j]);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float2 f = __bfloat1622float2(p[q]);
@@ -35,6 +33,17 @@ __device__ __forceinline__ uint4 combine_vec(Load load, const int64_t (&src)[kMa
 #pragma unroll
     for (int q = 0; q < 4; ++q) po[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
     return o;
+}
+
+// load(i): 16-byte vector i of y_sorted; src[j]: first vector of slot j's row.
+template <typename Load>
+__device__ __forceinline__ uint4 combine_vec(Load load, const int64_t (&src)[kMaxK],
+                                             const float (&g)[kMaxK], int k, int64_t v) {
+    uint4 r[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+        if (j < k) r[j] = load(src[j] + v);
+    return combine_vals(r, g, k);
 }
 
 }  // namespace moe

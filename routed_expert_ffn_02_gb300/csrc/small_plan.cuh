@@ -157,23 +157,36 @@ __device__ inline void combine_if_last(const SelfRoute& sr, const SmallPlan& sp,
 
 // Called by every thread of one block: out[t] for every token of the batch,
 // from y_sorted rows written by other CTAs of the same kernel (read through
-// L2) and the batch's gates and route lists in sp.
+// L2) and the batch's gates and route lists in sp.  The batch's T * H / 8
+// output vectors are taken two per thread per pass, with the 2k row loads of
+// both issued before either is summed (combine_vals: the combine kernel's
+// arithmetic).
 __device__ inline void combine_small(const SelfRoute& sr, const SmallPlan& sp,
                                      const __nv_bfloat16* y_sorted, int H) {
-    const int vec = H / 8;
+    const int vec = H / 8, k = sr.k;
+    const int n = sr.T * vec;
     const uint4* y = reinterpret_cast<const uint4*>(y_sorted);
     uint4* out = reinterpret_cast<uint4*>(sr.out);
-    auto load = [&](int64_t i) { return __ldcg(y + i); };
-    for (int t = 0; t < sr.T; ++t) {
-        int64_t src[kMaxK];
-        float g[kMaxK];
+    for (int i0 = threadIdx.x; i0 < n; i0 += 2 * (int)blockDim.x) {
+        const int i1 = i0 + (int)blockDim.x;
+        const bool two = i1 < n;
+        const int t0 = i0 / vec, v0 = i0 - t0 * vec;
+        const int t1 = two ? i1 / vec : t0, v1 = two ? i1 - t1 * vec : v0;
+        uint4 r0[kMaxK], r1[kMaxK];
+        float g0[kMaxK], g1[kMaxK];
 #pragma unroll
         for (int j = 0; j < kMaxK; ++j) {
-            src[j] = (j < sr.k) ? (int64_t)sp.inv_perm[t * sr.k + j] * vec : 0;
-            g[j] = (j < sr.k) ? sp.gates[t * sr.k + j] : 0.f;
+            if (j < k) {
+                r0[j] = __ldcg(y + (int64_t)sp.inv_perm[t0 * k + j] * vec + v0);
+                r1[j] = __ldcg(y + (int64_t)sp.inv_perm[t1 * k + j] * vec + v1);
+                g0[j] = sp.gates[t0 * k + j];
+                g1[j] = sp.gates[t1 * k + j];
+            } else {
+                g0[j] = g1[j] = 0.f;
+            }
         }
-        for (int v = threadIdx.x; v < vec; v += blockDim.x)
-            out[(int64_t)t * vec + v] = combine_vec(load, src, g, sr.k, v);
+        out[i0] = combine_vals(r0, g0, k);
+        if (two) out[i1] = combine_vals(r1, g1, k);
     }
 }
 
