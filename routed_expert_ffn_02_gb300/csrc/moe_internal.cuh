@@ -55,10 +55,15 @@ struct ThinUnit {
     int32_t cost_before;   // sum of thin_unit_cost over the preceding units
 };
 
-// Relative cost of one weight row of a unit with n slots on the streaming
-// path: flat while the row is bound by its HBM read, then growing with the
-// FMAs (used to split units' rows evenly over CTAs).
-__host__ __device__ inline int thin_unit_cost(int n) { return (n < 4 ? 4 : n) + 2; }
+// Relative cost of one weight row of a unit with n slots on the CUDA-core
+// streaming path (used to split units' rows evenly over CTAs).  Measured per
+// row with every SM streaming (full-size decode layers, batches 1-4): 1,
+// 1.05-1.07, 1.12-1.17 and 1.27-1.30 times a one-slot row for 1..4 slots
+// (register-cached rows, the FMAs partly hidden under the HBM read); beyond
+// 4 slots rows are read from shared memory and the cost grows with n.
+__host__ __device__ inline int thin_unit_cost(int n) {
+    return n <= 1 ? 20 : n == 2 ? 21 : n == 3 ? 23 : 13 * (n + 2) / 3;
+}
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
