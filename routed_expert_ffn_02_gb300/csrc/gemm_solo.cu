@@ -81,7 +81,12 @@ grouped_gemm_solo_kernel(const __grid_constant__ CUtensorMap tmA,
     grid_dep_wait();
     grid_dep_launch();
     const int total = args.hdr_ro->n_solo * args.n_blocks_n;
-    if ((int)blockIdx.x >= total) return;
+    // Items go round-robin to the first `active` CTAs, as many as keep every
+    // wave full: a last wave of a few items (8 of 464 at the prefill chunk)
+    // would stream alone at one SM's copy rate, well below its share of HBM.
+    const int waves = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int active = waves > 0 ? (total + waves - 1) / waves : 0;
+    if ((int)blockIdx.x >= active) return;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -115,7 +120,7 @@ grouped_gemm_solo_kernel(const __grid_constant__ CUtensorMap tmA,
         int pending[STAGES];
         for (int s = 0; s < STAGES; ++s) pending[s] = -1;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        for (int t = blockIdx.x; ok && t < total; t += active) {
             const FatTile ft = args.tiles[t / args.n_blocks_n];
             const int brow = weight_block(args.wslot, ft.expert) * args.b_rows_per_expert +
                              (t % args.n_blocks_n) * b_tile_rows;
@@ -154,7 +159,7 @@ grouped_gemm_solo_kernel(const __grid_constant__ CUtensorMap tmA,
         int it = 0;
         bool ok = true;
         bool issued = false;
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++it) {
+        for (int t = blockIdx.x; ok && t < total; t += active, ++it) {
             const int acc = it & 1;
             if (!mbar_wait_for(tempty_bar(acc), (uint32_t)((it >> 1) & 1) ^ 1u, args.wait_cycles, abort_flag)) {
                 ok = false;
@@ -198,7 +203,7 @@ grouped_gemm_solo_kernel(const __grid_constant__ CUtensorMap tmA,
         const int ew = warp - 4;   // TMEM lanes 32*ew .. 32*ew+31
         const int row = ew * 32 + lane;
         int it = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+        for (int t = blockIdx.x; t < total; t += active, ++it) {
             const int acc = it & 1;
             // the whole warp decides together (tcgen05.ld below is warp-wide)
             if (!__all_sync(0xffffffffu, mbar_wait_for(tfull_bar(acc), (uint32_t)((it >> 1) & 1), args.wait_cycles, abort_flag))) {
