@@ -333,20 +333,21 @@ def _forward_vs_entry_points(moe, s, shape, d, inp, launches):
 # router, route-list, gather and combine kernels (measured faster than routing
 # inside the streaming kernels at these sizes): six launches.
 PLANNED_MMA = [
-    # T, E, k, H, I, fat threshold
-    (12, 5, 3, 768, 512, 32),      # 36 slots on 5 experts (up to 12 slots each)
-    (20, 1024, 8, 256, 256, 32),   # 160 slots, E = 1024
-    (32, 64, 8, 512, 256, 33),     # 256 slots: the plan's capacity
-    (9, 40, 6, 1280, 768, 32),     # 54 slots, k = 6, H not a power of two
+    # T, E, k, H, I, fat threshold, launches
+    (12, 5, 3, 768, 512, 32, 6),      # 36 slots on 5 experts (up to 12 slots each)
+    (20, 1024, 8, 256, 256, 32, 6),   # 160 slots, E = 1024
+    (32, 64, 8, 512, 256, 33, 6),     # 256 slots: the plan's capacity
+    (9, 40, 6, 1280, 768, 32, 6),     # 54 slots, k = 6, H not a power of two
+    (32, 10, 8, 512, 256, 32, 10),    # two 32-slot (fat) experts beside thin ones: GEMMs too
 ]
 
 
-@pytest.mark.parametrize("T,E,k,H,I,thr", PLANNED_MMA)
-def test_forward_mma_batches_33_to_256_slots(moe, T, E, k, H, I, thr):
+@pytest.mark.parametrize("T,E,k,H,I,thr,launches", PLANNED_MMA)
+def test_forward_mma_batches_33_to_256_slots(moe, T, E, k, H, I, thr, launches):
     s = synth.Shape(T=T, E=E, k=k, H=H, I=I)
     inp = synth.make_layer(s, seed=300 + T, zipf_s=synth.ZIPF_S)
     shape = moe.Shape(T, E, k, H, I, fat_threshold=thr, thin_mma_min=MMA_ALL)
-    _forward_vs_entry_points(moe, s, shape, _to_dev(inp), inp, 6)
+    _forward_vs_entry_points(moe, s, shape, _to_dev(inp), inp, launches)
 
 
 @pytest.mark.parametrize("B", [5, 8, 16, 24])
