@@ -191,12 +191,23 @@ def stage_work(shape, counts_np):
     n_fat, n_thin = int(fat.sum()), int(thin.sum())
     w_gu = 2 * I * H * 2      # gate + up bytes per expert
     w_d = H * I * 2
+    # With fat experts the gather kernel copies the rows of the first third of
+    # the pair tiles (256-row tiles of experts with more than one 128-row
+    # tile, in expert order); the gate/up GEMM's first launch copies the rest.
+    pair_rows = []
+    for c in counts_np:
+        c = int(c)
+        if c >= max(thr, 1) and c > 128:
+            pair_rows += [min(256, c - 256 * q) for q in range((c + 255) // 256)]
+    gathered = fat_rows + mma_rows
+    first = sum(pair_rows[:(len(pair_rows) + 2) // 3]) if n_fat else gathered
     return {
         "route": dict(bytes=T * E * 4 + P * 8, flops=0),
         "permute": dict(bytes=P * 4 * 4 + E * 8, flops=0),
-        "gather": dict(bytes=(fat_rows + mma_rows) * H * 2 * 2, flops=0),
+        "gather": dict(bytes=first * H * 2 * 2, flops=0),
         "gemm_gate_up": dict(flops=2 * fat_rows * H * 2 * I,
-                             bytes=n_fat * w_gu + fat_rows * (H + I) * 2),
+                             bytes=n_fat * w_gu + fat_rows * (H + I) * 2
+                             + (gathered - first) * H * 2 * 2),
         "thin_gate_up": dict(bytes=n_thin * w_gu + thin_rows * (H + I) * 2,
                              flops=2 * thin_rows * H * 2 * I),
         "gemm_down": dict(flops=2 * fat_rows * I * H,
@@ -691,6 +702,10 @@ def run_gpu(args):
     dominant = max(stage_ms, key=stage_ms.get)
     roof = roofline_for(dominant, work, stage_ms[dominant], peaks)
     roof["kernel"] = dominant
+    if work["_info"]["fat_experts"]:
+        roof["note"] = ("the stage's first GEMM launch also copies two thirds of the row "
+                        "gather (the later pair tiles', solo and tensor-core tiles' x rows) "
+                        "with otherwise idle warps")
     roof["traffic"] = args.traffic if args.traffic is not None else (
         measured_traffic(dominant) if not (args.tokens or args.experts) else None)
     stages = {s: {"ms": round(stage_ms[s], 4), **{k2: v2 for k2, v2 in

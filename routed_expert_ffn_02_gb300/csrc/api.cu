@@ -296,15 +296,22 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
     const ExpertKernels kn = expert_kernels(sh, fat_bound);
     const int64_t ra = rows_alloc(P);
     const int H = sh->H, I = sh->I, sms = dev.num_sms;
+    // With fat experts the gather kernel copies only the rows of the first
+    // pair tiles; the gate/up GEMM launch over those tiles copies the rest
+    // with its idle warps, and a second launch runs the other pair tiles.
     if (kn.gather() && !sr) {   // a self-routed batch loads its x rows itself
         const Nvtx r("moe.gather");
-        CUDA_TRY(launch_gather(x, perm, sh->k, H, plan, x_sorted, sms, s), "gather");
+        CUDA_TRY(launch_gather(x, perm, sh->k, H, plan, x_sorted, sms, s, kn.fat ? 1 : 0),
+                 "gather");
     }
     CUDA_TRY(mark(ev, kEvGather, s), "cudaEventRecord");
     if (kn.fat) {
         const Nvtx r("moe.gemm_gate_up");
-        CUDA_TRY(launch_gemm_gate_up(x_sorted, ra, Wg, Wu, H, I, plan, h, sms, s),
+        CUDA_TRY(launch_gemm_gate_up(x_sorted, ra, Wg, Wu, H, I, plan, h, sms, s, 1, x, perm,
+                                     sh->k),
                  "grouped GEMM gate/up");
+        CUDA_TRY(launch_gemm_gate_up(x_sorted, ra, Wg, Wu, H, I, plan, h, sms, s, 2),
+                 "grouped GEMM gate/up (second part)");
         CUDA_TRY(launch_gemm_solo_gate_up(x_sorted, ra, Wg, Wu, H, I, plan, h, sms, s),
                  "grouped GEMM gate/up (solo tiles)");
     }
@@ -569,7 +576,8 @@ int32_t moe_forward_launches(const moe_shape* shape) {
     n += (P <= kPermChunk) ? 1 : 3;                  // route lists (+ planner)
     const ExpertKernels kn = expert_kernels(shape, shape->T);
     if (kn.gather()) n += 1;
-    if (kn.fat) n += 4;                              // grouped GEMMs (pairs, solo tiles)
+    if (kn.fat) n += 5;                              // grouped GEMMs (gate/up pairs in two
+                                                     // parts, down pairs, solo tiles)
     if (kn.units) n += 2;                            // CUDA-core streaming
     if (kn.mma) n += 2;                              // tensor-core streaming
     n += 1;                                          // combine

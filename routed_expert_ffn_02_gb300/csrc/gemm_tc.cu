@@ -31,6 +31,8 @@
 //               fp32 accumulators in TMEM, two 256-column buffers so the
 //               epilogue of one tile overlaps the main loop of the next;
 //   warp 2      TMEM allocator (both CTAs, collectively);
+//   warps 2-3   gate/up, first launch of a batch only: the row gather for
+//               the second launch (see below);
 //   warps 4-7   epilogue: tcgen05.ld -> activation -> bf16 -> a 128-byte-
 //               swizzled 32 x 64 shared tile per warp -> one TMA tensor store
 //               (coalesced 128-byte rows; per-lane stores of 16 bytes to 32
@@ -39,6 +41,15 @@
 //               end stores its valid rows itself.
 // Rows of a tile past the expert's end belong to other experts (or are past
 // the tensor and zero-filled by TMA); they are computed and discarded.
+//
+// The gate/up GEMM of a batch runs as two launches (GemmArgs::part): the
+// first over the first third of the pair tiles, whose x_sorted rows the
+// gather kernel copied, while its otherwise idle warps 2-3 copy the rows of
+// the other tiles (gather_dev.cuh); the second over the rest.  So two thirds
+// of the gather's HBM traffic run under tensor-bound work (prefill chunk:
+// 5.37-5.52 -> 5.28-5.42 ms per step, measured; a first part of a quarter or
+// a fifth left the idle warps too little time and stretched the first
+// launch).
 //
 // Every mbarrier wait is bounded (main-loop waits by GemmArgs::wait_cycles).
 // On expiry the role records MOE_ERR_TIMEOUT in the workspace status and
@@ -50,6 +61,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "gather_dev.cuh"
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
@@ -93,6 +105,9 @@ struct GemmArgs {
     __nv_bfloat16* out;    // [rows, ld_out]
     int64_t ld_out;
     long long wait_cycles; // limit of each main-loop wait (SM cycles)
+    int part;              // pair tiles: 0 all, 1 the first gather part (its idle
+                           // warps then gather the other rows), 2 the rest
+    GatherRows gather;     // part 1 of gate/up: the rows of part 2
 };
 
 // Stage rounds filled into stage s by a producer that filled `fills` stages
@@ -195,7 +210,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     grid_dep_launch();
 
     const int n_pairs = args.hdr_ro->n_fat_tiles >> 1;
-    const int total = n_pairs * args.n_blocks_n;
+    const int q_split = gather_first_pairs(n_pairs);
+    const int w0 = (args.part == 2 ? q_split : 0) * args.n_blocks_n;
+    const int total = (args.part == 1 ? q_split : n_pairs) * args.n_blocks_n;
+    const int w_first = w0 + cluster;
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer (both CTAs) ----------------
@@ -207,8 +225,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         bool ok = true;
         // Each item's tile is loaded one item ahead (its latency is hidden).
         FatTile ft_next = {};
-        if (cluster < total) ft_next = args.tiles[2 * (cluster / args.n_blocks_n) + (int)rank];
-        for (int w = cluster; ok && w < total; w += n_clusters) {
+        if (w_first < total) ft_next = args.tiles[2 * (w_first / args.n_blocks_n) + (int)rank];
+        for (int w = w_first; ok && w < total; w += n_clusters) {
             const int nt = w % args.n_blocks_n;
             const FatTile ft = ft_next;
             if (w + n_clusters < total)
@@ -248,7 +266,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         int it = 0;
         bool ok = true;
         bool issued = false;
-        for (int w = cluster; ok && w < total; w += n_clusters, ++it) {
+        for (int w = w_first; ok && w < total; w += n_clusters, ++it) {
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)((it >> 1) & 1);
             if (!mbar_wait_for(tempty_bar(acc), acc_phase ^ 1u, args.wait_cycles, abort_flag)) {
@@ -291,6 +309,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 (void)mbar_wait(done_bar, 0);
             }
         }
+    } else if (kGated && args.part == 1 && (warp == 2 || warp == 3)) {
+        // ---------------- gather of the later pair tiles' rows ----------------
+        // (the next launch's A rows; this launch's tiles were gathered before)
+        int64_t r_beg, r_end;
+        gather_part_rows(args.hdr_ro, 2, &r_beg, &r_end);
+        gather_rows(args.gather, args.hdr_ro, r_beg, r_end,
+                    (int64_t)blockIdx.x * 2 + (warp - 2), (int64_t)gridDim.x * 2);
     } else if (warp >= 4) {
         // ---------------- epilogue (both CTAs) ----------------
         const int ew = warp - 4;              // TMEM lanes 32*ew .. 32*ew+31
@@ -300,8 +325,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         const uint32_t tempty0 = mapa_shared(tempty_bar(0), 0);
         int it = 0;
         FatTile ft_next = {};
-        if (cluster < total) ft_next = args.tiles[2 * (cluster / args.n_blocks_n) + (int)rank];
-        for (int w = cluster; w < total; w += n_clusters, ++it) {
+        if (w_first < total) ft_next = args.tiles[2 * (w_first / args.n_blocks_n) + (int)rank];
+        for (int w = w_first; w < total; w += n_clusters, ++it) {
             const FatTile ft = ft_next;
             if (w + n_clusters < total)
                 ft_next = args.tiles[2 * ((w + n_clusters) / args.n_blocks_n) + (int)rank];
@@ -473,7 +498,8 @@ cudaError_t make_tma_map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, ui
 cudaError_t launch_gemm_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_alloc,
                                 const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int H, int I,
                                 const Plan& plan, __nv_bfloat16* h, int num_sms,
-                                cudaStream_t s) {
+                                cudaStream_t s, int part, const __nv_bfloat16* x,
+                                const int32_t* perm, int k) {
     CUtensorMap mA, mG, mU;
     cudaError_t e;
     if ((e = make_tma_map_bf16(&mA, x_sorted, (uint64_t)rows_alloc, (uint64_t)H, BM)) != cudaSuccess) return e;
@@ -497,6 +523,15 @@ cudaError_t launch_gemm_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_allo
     a.out = h;
     a.ld_out = I;
     a.wait_cycles = main_wait_cycles();
+    a.part = part;
+    a.gather.x = reinterpret_cast<const uint4*>(x);
+    a.gather.perm = perm;
+    a.gather.k = k;
+    a.gather.vec = H / 8;
+    a.gather.tiles = plan.tiles;
+    a.gather.solo_tiles = plan.solo_tiles;
+    a.gather.mma_tiles = plan.mma_tiles;
+    a.gather.x_sorted = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(x_sorted));
     return launch_pdl(grouped_gemm_kernel<true>, dim3(grid), dim3(256), SMEM_BYTES, s, mA, mG, mU,
                       mO, a);
 }
@@ -526,6 +561,8 @@ cudaError_t launch_gemm_down(const __nv_bfloat16* h, int64_t rows_alloc,
     a.out = y_sorted;
     a.ld_out = H;
     a.wait_cycles = main_wait_cycles();
+    a.part = 0;
+    a.gather = GatherRows{};
     return launch_pdl(grouped_gemm_kernel<false>, dim3(grid), dim3(256), SMEM_BYTES, s, mA, mD,
                       mD, mO, a);
 }

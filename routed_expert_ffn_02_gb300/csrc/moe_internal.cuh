@@ -18,6 +18,11 @@ constexpr int kMaxK = 8;             // experts per token
 constexpr int kMaxE = 1024;          // experts per layer
 constexpr int kThinMaxTokens = 32;   // slots one weight-streaming expert may hold
 constexpr int kPermChunk = 2048;     // slots per block in the route-list kernels
+// The row gather of a batch with fat experts runs in two parts: the gather
+// kernel copies the rows of the first 1/kGatherFirstDen of the pair tiles;
+// the gate/up GEMM launch over those tiles copies the other rows with its
+// idle warps, for the second launch over the other pair tiles.
+constexpr int kGatherFirstDen = 3;
 constexpr int kTileM = 128;          // rows (slots) per grouped-GEMM tile
 constexpr int kMaxHidden = 16384;    // H and I (a weight-streaming stage holds a row)
 
@@ -54,6 +59,11 @@ struct ThinUnit {
     int32_t n;
     int32_t cost_before;   // sum of thin_unit_cost over the preceding units
 };
+
+// Pair tiles of the first gather part (of n_pairs).
+__host__ __device__ inline int gather_first_pairs(int n_pairs) {
+    return (n_pairs + kGatherFirstDen - 1) / kGatherFirstDen;
+}
 
 // Relative cost of one weight row of a unit with n slots on the CUDA-core
 // streaming path (used to split units' rows evenly over CTAs).  Measured per
@@ -213,9 +223,11 @@ size_t permute_scratch_ints(int64_t P, int E);   // chunk_hist + chunk_base
 cudaError_t launch_plan(const int32_t* counts, const int32_t* offsets, int E,
                         const Plan& plan, cudaStream_t s);
 
+// part: 0 every row; 1 the rows of the first gather_first_pairs() pair
+// tiles; 2 the other rows (the later pair tiles, solo and tensor-core tiles).
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* perm, int k,
                           int H, const Plan& plan, __nv_bfloat16* x_sorted,
-                          int num_sms, cudaStream_t s);
+                          int num_sms, cudaStream_t s, int part = 0);
 
 // max_slots: an upper bound of any expert's slot count (sizes the staged
 // activation buffer; units never hold more than plan.unit_tokens).
@@ -268,10 +280,14 @@ cudaError_t launch_gemm_solo_down(const __nv_bfloat16* h, int64_t rows_alloc,
 
 // Grouped GEMMs on tcgen05.  gate_up: h = silu(A Wg^T) * (A Wu^T) for the
 // fat tiles, A = x_sorted [rows_alloc, H].  down: y = h Wd^T, A = h.
+// gate_up part: 0 every pair tile; 1 the first gather_first_pairs() pair
+// tiles, the launch also gathering the gather's part-2 rows from x (by perm
+// and k) into x_sorted; 2 the other pair tiles.
 cudaError_t launch_gemm_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_alloc,
                                 const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int H, int I,
                                 const Plan& plan, __nv_bfloat16* h, int num_sms,
-                                cudaStream_t s);
+                                cudaStream_t s, int part = 0, const __nv_bfloat16* x = nullptr,
+                                const int32_t* perm = nullptr, int k = 0);
 cudaError_t launch_gemm_down(const __nv_bfloat16* h, int64_t rows_alloc,
                              const __nv_bfloat16* Wd, int H, int I, const Plan& plan,
                              __nv_bfloat16* y_sorted, int num_sms, cudaStream_t s);

@@ -17,6 +17,7 @@
 //           inside a warp come from __match_any_sync, so the order of slots
 //           of one expert is kept.
 // Small inputs (decode) take one single-block kernel doing all of it.
+#include "gather_dev.cuh"
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 
@@ -381,42 +382,17 @@ plan_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ offs
 }
 
 // x_sorted[p] = x[perm[p] / k] for the rows of the fat tiles (paired and
-// solo) and of the tensor-core streaming tiles; one warp per row, 16-byte
-// vectors.
+// solo) and of the tensor-core streaming tiles (all of them, or one of the
+// two gather parts); one warp per row, 16-byte vectors.
 __global__ void __launch_bounds__(256)
-gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
-              int k, int H, const FatTile* __restrict__ tiles,
-              const FatTile* __restrict__ solo_tiles, const FatTile* __restrict__ mma_tiles,
-              const WsHeader* __restrict__ hdr, uint4* __restrict__ x_sorted) {
+gather_kernel(GatherRows g, const WsHeader* __restrict__ hdr, int part) {
     ptx::grid_dep_wait();
     ptx::grid_dep_launch();
-    const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    const int64_t fat_rows = (int64_t)hdr->n_fat_tiles * kTileM;
-    const int64_t solo_rows = fat_rows + (int64_t)hdr->n_solo * kTileM;
-    const int64_t rows = solo_rows + (int64_t)hdr->n_thin_mma * kThinMaxTokens;
-    const int vec = H / 8;
-    for (int64_t r = warp; r < rows; r += nwarps) {
-        FatTile ft;
-        int i;
-        if (r < fat_rows) {
-            ft = tiles[r / kTileM];
-            i = (int)(r % kTileM);
-        } else if (r < solo_rows) {
-            ft = solo_tiles[(r - fat_rows) / kTileM];
-            i = (int)((r - fat_rows) % kTileM);
-        } else {
-            ft = mma_tiles[(r - solo_rows) / kThinMaxTokens];
-            i = (int)((r - solo_rows) % kThinMaxTokens);
-        }
-        if (i >= ft.rows) continue;
-        const int64_t p = ft.row0 + i;
-        const int64_t t = perm[p] / k;
-        const uint4* src = x + t * vec;
-        uint4* dst = x_sorted + p * vec;
-        for (int v = lane; v < vec; v += 32) dst[v] = __ldg(src + v);
-    }
+    int64_t r_beg, r_end;
+    gather_part_rows(hdr, part, &r_beg, &r_end);
+    gather_rows(g, hdr, r_beg, r_end, warp, nwarps);
 }
 
 }  // namespace
@@ -458,10 +434,18 @@ cudaError_t launch_plan(const int32_t* counts, const int32_t* offsets, int E,
 
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* perm, int k,
                           int H, const Plan& plan, __nv_bfloat16* x_sorted,
-                          int num_sms, cudaStream_t s) {
-    return launch_pdl(gather_kernel, dim3(num_sms * 8), dim3(256), 0, s,
-                      reinterpret_cast<const uint4*>(x), perm, k, H, plan.tiles, plan.solo_tiles,
-                      plan.mma_tiles, plan.hdr, reinterpret_cast<uint4*>(x_sorted));
+                          int num_sms, cudaStream_t s, int part) {
+    GatherRows g;
+    g.x = reinterpret_cast<const uint4*>(x);
+    g.perm = perm;
+    g.k = k;
+    g.vec = H / 8;
+    g.tiles = plan.tiles;
+    g.solo_tiles = plan.solo_tiles;
+    g.mma_tiles = plan.mma_tiles;
+    g.x_sorted = reinterpret_cast<uint4*>(x_sorted);
+    return launch_pdl(gather_kernel, dim3(num_sms * 8), dim3(256), 0, s, g,
+                      (const WsHeader*)plan.hdr, part);
 }
 
 }  // namespace moe

@@ -155,18 +155,18 @@ def test_forward_launch_count(moe):
     for B in (5, 8, 16, 24):                                 # decode sweep: > 32 slots
         assert moe.forward_launches(S(B, 384, 8, 4096, 2048)) == 6
     assert moe.forward_launches(S(32, 64, 8, 512, 256, 33, 1)) == 6   # 256 slots
-    assert moe.forward_launches(S(32, 64, 8, 512, 256, 32, 1)) == 10  # T = 32 may be fat
+    assert moe.forward_launches(S(32, 64, 8, 512, 256, 32, 1)) == 11  # T = 32 may be fat
     # CUDA-core self-routing limits: 32 slots, below the fat threshold, one
     # unit per expert
     assert moe.forward_launches(S(5, 384, 8, 4096, 2048, thin_mma_min=33)) == 5   # 40 slots
-    assert moe.forward_launches(S(32, 64, 1, 512, 256, thin_mma_min=33)) == 10    # T = 32 may be fat
+    assert moe.forward_launches(S(32, 64, 1, 512, 256, thin_mma_min=33)) == 11    # T = 32 may be fat
     assert moe.forward_launches(S(16, 64, 2, 512, 256, thin_mma_min=33)) == 1     # unit of 16
     assert moe.forward_launches(S(13, 64, 2, 4096, 2048, thin_mma_min=33)) == 5   # units of 12
-    assert moe.forward_launches(S(2, 64, 2, 512, 256, fat_threshold=0)) == 8     # every expert fat
-    # fat experts: pair GEMMs and solo-tile GEMMs for gate/up and down
-    assert moe.forward_launches(S(16384, 384, 8, 4096, 2048)) == 12
-    assert moe.forward_launches(S(16384, 384, 8, 4096, 2048, thin_mma_min=8)) == 14
-    assert moe.forward_launches(S(16384, 384, 8, 4096, 2048, fat_threshold=0)) == 10
+    assert moe.forward_launches(S(2, 64, 2, 512, 256, fat_threshold=0)) == 9     # every expert fat
+    # fat experts: pair GEMMs (gate/up in two launches) and solo-tile GEMMs
+    assert moe.forward_launches(S(16384, 384, 8, 4096, 2048)) == 13
+    assert moe.forward_launches(S(16384, 384, 8, 4096, 2048, thin_mma_min=8)) == 15
+    assert moe.forward_launches(S(16384, 384, 8, 4096, 2048, fat_threshold=0)) == 11
     assert moe.forward_launches(S(0, 384, 8, 4096, 2048)) == 0
 
 

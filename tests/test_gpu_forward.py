@@ -338,7 +338,7 @@ PLANNED_MMA = [
     (20, 1024, 8, 256, 256, 32, 6),   # 160 slots, E = 1024
     (32, 64, 8, 512, 256, 33, 6),     # 256 slots: the plan's capacity
     (9, 40, 6, 1280, 768, 32, 6),     # 54 slots, k = 6, H not a power of two
-    (32, 10, 8, 512, 256, 32, 10),    # two 32-slot (fat) experts beside thin ones: GEMMs too
+    (32, 10, 8, 512, 256, 32, 11),    # two 32-slot (fat) experts beside thin ones: GEMMs too
 ]
 
 
