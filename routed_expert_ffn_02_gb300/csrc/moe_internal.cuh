@@ -35,8 +35,9 @@ struct WsHeader {
     int32_t n_thin_mma;    // thin experts on the tensor-core streaming kernel
     int32_t n_solo;        // fat experts' leftover 128-row tiles (one-CTA GEMM)
     int32_t ticket;        // CTAs of a streaming down kernel done (fused combine)
-    uint32_t layer_sync;   // CTAs past the gate/up phase of the one-kernel decode layer
-                           // (monotonic: a launch waits for its own multiple of the grid)
+    uint32_t layer_sync;   // grid-wide waits of the one-kernel decode layer (after gate/up,
+                           // before the combine): CTA arrivals, monotonic; each wait
+                           // ends at the next multiple of the grid size
     int32_t reserved[56];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
