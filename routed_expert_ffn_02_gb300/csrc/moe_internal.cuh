@@ -131,6 +131,33 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// launch_pdl, and with coop also a cooperative launch (every block resident
+// at once, or the launch fails): for kernels whose blocks wait on one another.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_coop(bool coop, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                            size_t smem, cudaStream_t s, Args&&... args) {
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (t_pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (coop) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Planner outputs (the split of experts between the expert kernels).  A thin
 // expert (0 < count < fat_threshold) with at least thin_mma_min slots streams
 // its weights through the tensor cores (one FatTile of <= kThinMaxTokens rows

@@ -784,54 +784,6 @@ __device__ __forceinline__ void smem_teardown(const Smem& m) {
     }
 }
 
-// The combine of a cooperative launch (every CTA resident): each CTA fences
-// its y rows and arrives on the workspace's layer_sync counter (monotonic,
-// like the layer's first grid-wide wait); thread 0 waits, bounded, for the
-// whole grid, and then the CTA combines its own share of the batch's T*H/8
-// output vectors with the combine kernel's arithmetic (combine_vals).  Each
-// CTA loads a few vectors once, instead of one CTA loading all of them.
-__device__ inline void combine_spread(const SelfRoute& sr, const SmallPlan& sp, WsHeader* hdr,
-                                      const __nv_bfloat16* y_sorted, int H,
-                                      long long wait_cycles) {
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const uint32_t seen = atomicAdd(&hdr->layer_sync, 1u);
-        const uint32_t target = (seen / gridDim.x + 1) * gridDim.x;
-        const long long t0 = clock64();
-        while ((int32_t)(ld_acquire_gpu(&hdr->layer_sync) - target) < 0) {
-            if (clock64() - t0 > wait_cycles) {
-                set_status(hdr, MOE_ERR_TIMEOUT);
-                break;
-            }
-            __nanosleep(32);
-        }
-        __threadfence();
-    }
-    __syncthreads();
-    const int vec = H / 8, k = sr.k;
-    const int n = sr.T * vec;
-    const int i_end = (int)((int64_t)n * (blockIdx.x + 1) / gridDim.x);
-    const uint4* y = reinterpret_cast<const uint4*>(y_sorted);
-    uint4* out = reinterpret_cast<uint4*>(sr.out);
-    for (int i = (int)((int64_t)n * blockIdx.x / gridDim.x) + (int)threadIdx.x; i < i_end;
-         i += (int)blockDim.x) {
-        const int t = i / vec, v = i - t * vec;
-        uint4 r[kMaxK];
-        float g[kMaxK];
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j) {
-            if (j < k) {
-                r[j] = __ldcg(y + (int64_t)sp.inv_perm[t * k + j] * vec + v);
-                g[j] = sp.gates[t * k + j];
-            } else {
-                g[j] = 0.f;
-            }
-        }
-        out[i] = combine_vals(r, g, k);
-    }
-}
-
 // One decode layer of a self-routed batch in one cooperative launch (every
 // CTA resident at once, one per SM):
 //   1. gate/up: routing, route lists and units in every CTA (CTA 0 stores

@@ -26,7 +26,8 @@
 // expert, and loads each tile's activation rows straight from x with one-row
 // TMA boxes (the 128-byte swizzle follows the shared-memory address, so a row
 // lands where a 32-row box would put it), so no gather runs; the down kernel
-// reads the plan back and its last CTA combines the batch.
+// reads the plan back and, launched cooperatively, every CTA combines its
+// share of the batch after a bounded grid-wide wait (combine_spread).
 //
 // Persistent, one CTA per SM, warp-specialised like the grouped GEMM:
 // warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM allocator, warps 4-7
@@ -302,7 +303,9 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
         fence_after();
         tmem_dealloc(tmem_base, C::kTmemCols);
     }
-    if (!kGated && self && args.sr.out) combine_if_last(args.sr, sp, args.hdr, args.out, (int)args.ld_out);
+    // self-routed: a cooperative launch, so every CTA combines its share
+    if (!kGated && self && args.sr.out)
+        combine_spread(args.sr, sp, args.hdr, args.out, (int)args.ld_out, args.wait_cycles);
 }
 
 template <bool kGated>
@@ -363,8 +366,10 @@ cudaError_t launch_thin_mma_down(const __nv_bfloat16* h, int64_t rows_alloc,
     a.ld_out = H;
     a.wait_cycles = main_wait_cycles();
     a.sr = sr ? *sr : SelfRoute{};
-    return launch_pdl(thin_mma_kernel<false>, dim3(num_sms), dim3(256), Cfg<false>::kSmemBytes, s,
-                      mX, mD, mD, mX, a);
+    // a self-routed batch's CTAs wait for one another before the combine:
+    // every CTA resident at once
+    return launch_pdl_coop(sr != nullptr, thin_mma_kernel<false>, dim3(num_sms), dim3(256),
+                           Cfg<false>::kSmemBytes, s, mX, mD, mD, mX, a);
 }
 
 }  // namespace moe
