@@ -291,7 +291,8 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
                        const __nv_bfloat16* Wd, __nv_bfloat16* x_sorted,
                        __nv_bfloat16* h, __nv_bfloat16* y, const Plan& plan,
                        int64_t fat_bound, cudaStream_t s, cudaEvent_t* ev,
-                       const SelfRoute* sr = nullptr) {
+                       const SelfRoute* sr = nullptr, const SelfRoute* comb = nullptr,
+                       bool* combined = nullptr) {
     const int64_t P = (int64_t)sh->T * sh->k;
     const ExpertKernels kn = expert_kernels(sh, fat_bound);
     const int64_t ra = rows_alloc(P);
@@ -347,9 +348,13 @@ moe_status run_experts(const moe_shape* sh, const DeviceInfo& dev, const __nv_bf
         const Nvtx r("moe.thin_down");
         if (kn.units && !one_launch)
             CUDA_TRY(launch_thin_down(h, H, I, Wd, plan, fat_bound, y, sms, s, sr), "thin down");
+        // A planned batch whose only expert kernel is the tensor-core one
+        // combines in that kernel's down launch (comb: its route lists).
+        const bool fuse = comb && !sr && kn.mma && !kn.fat && !kn.units;
         if (kn.mma)
-            CUDA_TRY(launch_thin_mma_down(h, ra, Wd, H, I, plan, y, sms, s, sr),
+            CUDA_TRY(launch_thin_mma_down(h, ra, Wd, H, I, plan, y, sms, s, fuse ? comb : sr),
                      "thin down (tensor cores)");
+        if (combined) *combined = fuse;
     }
     CUDA_TRY(mark(ev, kEvThinDown, s), "cudaEventRecord");
     return MOE_OK;
@@ -519,11 +524,14 @@ static moe_status forward_impl(const moe_shape* shape, const float* logits, cons
     // The router sends a token to k distinct experts, so no expert holds more
     // than T slots.  x_sorted is dead once the gate/up GEMM is done, so
     // y_sorted reuses its storage.
+    const SelfRoute comb{nullptr, T, E, k, idx, g, b.counts, b.offsets, b.perm, b.inv_perm,
+                         b.units, (__nv_bfloat16*)out};
+    bool combined = false;
     st = run_experts(shape, dev, (const __nv_bfloat16*)x, b.perm, (const __nv_bfloat16*)W_gate,
                      (const __nv_bfloat16*)W_up, (const __nv_bfloat16*)W_down, b.xy, b.h, b.xy,
-                     plan, T, s, ev, self ? &sr : nullptr);
+                     plan, T, s, ev, self ? &sr : nullptr, &comb, &combined);
     if (st != MOE_OK) return st;
-    if (!self) {
+    if (!self && !combined) {
         const Nvtx r("moe.combine");
         CUDA_TRY(launch_combine(b.xy, b.inv_perm, g, T, k, shape->H, (__nv_bfloat16*)out,
                                 dev.num_sms, s), "combine");
@@ -580,7 +588,7 @@ int32_t moe_forward_launches(const moe_shape* shape) {
                                                      // parts, down pairs, solo tiles)
     if (kn.units) n += 2;                            // CUDA-core streaming
     if (kn.mma) n += 2;                              // tensor-core streaming
-    n += 1;                                          // combine
+    if (kn.fat || kn.units || !kn.mma) n += 1;       // combine (else fused into the last)
     return n;
 }
 

@@ -291,6 +291,10 @@ cudaError_t launch_thin_mma_gate_up(const __nv_bfloat16* x_sorted, int64_t rows_
                                     int I, const Plan& plan, __nv_bfloat16* h, int num_sms,
                                     cudaStream_t s, const SelfRoute* sr = nullptr,
                                     const __nv_bfloat16* x = nullptr);
+// down with sr->out set: the combine is fused (a cooperative launch; every
+// CTA combines its share of out after a bounded grid-wide wait), by the
+// batch's own plan (sr->logits set) or, for a planned batch whose only expert
+// kernel this is, by sr's route lists (inv_perm, gates; sr->logits null).
 cudaError_t launch_thin_mma_down(const __nv_bfloat16* h, int64_t rows_alloc,
                                  const __nv_bfloat16* Wd, int H, int I, const Plan& plan,
                                  __nv_bfloat16* y_sorted, int num_sms, cudaStream_t s,

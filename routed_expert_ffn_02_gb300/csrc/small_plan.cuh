@@ -212,11 +212,13 @@ __device__ inline void combine_if_last(const SelfRoute& sr, const SmallPlan& sp,
 
 // The combine of a cooperative launch (every CTA resident): each CTA fences
 // its y rows and arrives on the workspace's layer_sync counter (monotonic,
-// like the layer's first grid-wide wait); thread 0 waits, bounded, for the
-// whole grid, and then the CTA combines its own share of the batch's T*H/8
-// output vectors with the combine kernel's arithmetic (combine_vals).  Each
-// CTA loads a few vectors once, instead of one CTA loading all of them.
-__device__ inline void combine_spread(const SelfRoute& sr, const SmallPlan& sp, WsHeader* hdr,
+// like the one-launch layer's first grid-wide wait); thread 0 waits, bounded,
+// for the whole grid, and then the CTA combines its own share of the batch's
+// T*H/8 output vectors with the combine kernel's arithmetic (combine_vals).
+// Each CTA loads a few vectors once, instead of one CTA loading all of them.
+// inv_perm / gates: [T*k], shared (the batch's own plan) or global memory.
+__device__ inline void combine_spread(const SelfRoute& sr, const int32_t* inv_perm,
+                                      const float* gates, WsHeader* hdr,
                                       const __nv_bfloat16* y_sorted, int H,
                                       long long wait_cycles) {
     __threadfence();
@@ -248,8 +250,8 @@ __device__ inline void combine_spread(const SelfRoute& sr, const SmallPlan& sp, 
 #pragma unroll
         for (int j = 0; j < kMaxK; ++j) {
             if (j < k) {
-                r[j] = __ldcg(y + (int64_t)sp.inv_perm[t * k + j] * vec + v);
-                g[j] = sp.gates[t * k + j];
+                r[j] = __ldcg(y + (int64_t)inv_perm[t * k + j] * vec + v);
+                g[j] = gates[t * k + j];
             } else {
                 g[j] = 0.f;
             }

@@ -924,7 +924,7 @@ thin_layer_kernel(const __nv_bfloat16* __restrict__ x, int k, int H, int I, int 
         }
         if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
     }
-    combine_spread(sr, sp, hdr, y, H, wait_cycles);
+    combine_spread(sr, sp.inv_perm, sp.gates, hdr, y, H, wait_cycles);
 }
 
 // Rows per item so that a weight slot holds at most kStageTarget bytes (at

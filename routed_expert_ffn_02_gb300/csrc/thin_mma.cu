@@ -303,9 +303,12 @@ thin_mma_kernel(const __grid_constant__ CUtensorMap tmX,
         fence_after();
         tmem_dealloc(tmem_base, C::kTmemCols);
     }
-    // self-routed: a cooperative launch, so every CTA combines its share
-    if (!kGated && self && args.sr.out)
-        combine_spread(args.sr, sp, args.hdr, args.out, (int)args.ld_out, args.wait_cycles);
+    // a fused combine (a cooperative launch): every CTA combines its share,
+    // by the batch's own plan or the planned route lists
+    if (!kGated && args.sr.out)
+        combine_spread(args.sr, self ? sp.inv_perm : args.sr.inv_perm,
+                       self ? sp.gates : args.sr.gates, args.hdr, args.out, (int)args.ld_out,
+                       args.wait_cycles);
 }
 
 template <bool kGated>
@@ -366,9 +369,9 @@ cudaError_t launch_thin_mma_down(const __nv_bfloat16* h, int64_t rows_alloc,
     a.ld_out = H;
     a.wait_cycles = main_wait_cycles();
     a.sr = sr ? *sr : SelfRoute{};
-    // a self-routed batch's CTAs wait for one another before the combine:
-    // every CTA resident at once
-    return launch_pdl_coop(sr != nullptr, thin_mma_kernel<false>, dim3(num_sms), dim3(256),
+    // with the combine fused the CTAs wait for one another before it: every
+    // CTA resident at once
+    return launch_pdl_coop(sr != nullptr && sr->out != nullptr, thin_mma_kernel<false>, dim3(num_sms), dim3(256),
                            Cfg<false>::kSmemBytes, s, mX, mD, mD, mX, a);
 }
 

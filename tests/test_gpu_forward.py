@@ -330,14 +330,15 @@ def _forward_vs_entry_points(moe, s, shape, d, inp, launches):
 
 
 # Batches of 33..256 slots on the tensor-core streaming kernel run the
-# router, route-list, gather and combine kernels (measured faster than routing
-# inside the streaming kernels at these sizes): six launches.
+# router, route-list and gather kernels (measured faster than routing inside
+# the streaming kernels at these sizes) and combine in the down kernel (a
+# cooperative launch): five launches.
 PLANNED_MMA = [
     # T, E, k, H, I, fat threshold, launches
-    (12, 5, 3, 768, 512, 32, 6),      # 36 slots on 5 experts (up to 12 slots each)
-    (20, 1024, 8, 256, 256, 32, 6),   # 160 slots, E = 1024
-    (32, 64, 8, 512, 256, 33, 6),     # 256 slots: the plan's capacity
-    (9, 40, 6, 1280, 768, 32, 6),     # 54 slots, k = 6, H not a power of two
+    (12, 5, 3, 768, 512, 32, 5),      # 36 slots on 5 experts (up to 12 slots each)
+    (20, 1024, 8, 256, 256, 32, 5),   # 160 slots, E = 1024
+    (32, 64, 8, 512, 256, 33, 5),     # 256 slots: the plan's capacity
+    (9, 40, 6, 1280, 768, 32, 5),     # 54 slots, k = 6, H not a power of two
     (32, 10, 8, 512, 256, 32, 11),    # two 32-slot (fat) experts beside thin ones: GEMMs too
 ]
 
@@ -360,7 +361,7 @@ def test_forward_decode_sweep_batches(moe, big_layer, B):
                logits=synth.make_logits(B, s.E, seed=400 + B, zipf_s=synth.ZIPF_S))
     d = dict(_to_dev(inp), **big_layer)
     shape = moe.Shape(B, s.E, s.k, s.H, s.I)
-    _forward_vs_entry_points(moe, s, shape, d, inp, 6)
+    _forward_vs_entry_points(moe, s, shape, d, inp, 5)
 
 
 @pytest.mark.parametrize("B,mma_min", [(1, 0), (2, 0), (4, MMA_NONE)])
