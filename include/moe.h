@@ -195,9 +195,11 @@ size_t moe_workspace_size(const moe_shape* shape);
  * initialised once with moe_workspace_init().  Batches of at most 32 token
  * slots whose experts all stream on one weight-streaming kernel (decode) run
  * as two kernels that route and combine inside themselves, or, on the
- * CUDA-core kernel at H = 4096, I = 2048 and H = 512, I = 256, as one
- * cooperative kernel (one CTA per SM) that also waits, bounded, between its
- * gate/up and down phases for every CTA; the results, topk_idx and gates
+ * CUDA-core kernel at (H, I) = (4096, 2048), (2048, 1024) and (512, 256), as
+ * one cooperative kernel (one CTA per SM) whose CTAs also wait, bounded, for
+ * one another after the gate/up phase and before the combine (the
+ * tensor-core kernel's down launch is cooperative too and waits likewise
+ * before its combine); the results, topk_idx and gates
  * included, are bit-identical to the separate stages.  Calls that share a
  * workspace must be ordered on one stream (or otherwise serialised). */
 moe_status moe_forward(const moe_shape* shape, const float* logits,

@@ -64,7 +64,8 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if force:
         for f in os.listdir(BUILD):
             os.remove(os.path.join(BUILD, f))
-    with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
+    workers = min(max(os.cpu_count() or 1, 8), len(srcs))
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose_ptxas=verbose_ptxas), srcs))
     newest = max(os.path.getmtime(o) for o in objs)
     if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < newest:

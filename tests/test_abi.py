@@ -139,8 +139,8 @@ def test_forward_launch_count(moe):
     only the expert kernels that can have work, then combine (fused into the
     tensor-core down kernel when that is the only expert kernel).  Small batches
     on one streaming kernel route inside it and combine in the down kernel:
-    gate/up, down; on the CUDA-core kernel at H=4096, I=2048 or H=512,
-    I=256, one cooperative launch for the whole layer."""
+    gate/up, down; on the CUDA-core kernel at H=4096, I=2048, H=2048,
+    I=1024 or H=512, I=256, one cooperative launch for the whole layer."""
     S = moe.Shape
     # decode: 8 or 16 touched experts x 16 blocks < 384 items -> CUDA cores,
     # from 24 x 16 = 384 on tensor cores; up to 32 slots the batch is routed
@@ -151,7 +151,8 @@ def test_forward_launch_count(moe):
     assert moe.forward_launches(S(4, 384, 8, 4096, 2048)) == 2
     assert moe.forward_launches(S(1, 384, 8, 4096, 2048, thin_mma_min=1)) == 2
     assert moe.forward_launches(S(4, 384, 8, 4096, 2048, thin_mma_min=33)) == 1
-    assert moe.forward_launches(S(2, 384, 8, 2048, 1024)) == 2    # no one-launch build
+    assert moe.forward_launches(S(2, 384, 8, 2048, 1024)) == 1
+    assert moe.forward_launches(S(2, 384, 8, 1024, 512)) == 2     # no one-launch build
     assert moe.forward_launches(S(4, 384, 8, 4096, 2048, thin_mma_min=3)) == 8   # split kernels
     for B in (5, 8, 16, 24):                                 # decode sweep: > 32 slots
         assert moe.forward_launches(S(B, 384, 8, 4096, 2048)) == 5

@@ -27,9 +27,12 @@ def test_stage_work_by_hand():
     H, I = 256, 128
     assert w["route"]["bytes"] == 4 * 8 * 4 + 8 * 8
     assert w["permute"]["bytes"] == 8 * 16 + 8 * 8
-    assert w["gather"]["bytes"] == (3 + 4) * H * 4
+    # no pair tiles (expert 0 is a single-tile solo expert): the gather
+    # kernel copies nothing, the gate/up GEMM's first launch copies all 7 rows
+    assert w["gather"]["bytes"] == 0
     assert w["gemm_gate_up"]["flops"] == 2 * 3 * H * 2 * I
-    assert w["gemm_gate_up"]["bytes"] == 1 * (2 * I * H * 2) + 3 * (H + I) * 2
+    assert w["gemm_gate_up"]["bytes"] == (1 * (2 * I * H * 2) + 3 * (H + I) * 2
+                                          + (3 + 4) * H * 4)
     assert w["gemm_down"]["flops"] == 2 * 3 * I * H
     assert w["gemm_down"]["bytes"] == 1 * (H * I * 2) + 3 * (H + I) * 2
     assert w["thin_gate_up"]["bytes"] == 3 * (2 * I * H * 2) + 5 * (H + I) * 2
@@ -37,6 +40,20 @@ def test_stage_work_by_hand():
     assert w["combine"]["bytes"] == 8 * H * 2 + 4 * H * 2 + 8 * 8
     assert w["_info"] == dict(fat_experts=1, thin_experts=3, fat_rows=3, thin_rows=5,
                               touched=4)
+
+
+def test_stage_work_gather_parts():
+    # Experts 0 and 1 are fat with 600 and 300 slots: pair tiles of 256 rows
+    # (expert 0: 256, 256, 88; expert 1: 256, 44), five pairs; the gather
+    # kernel copies the first ceil(5 / 3) = 2 pairs' rows (512), the first
+    # gate/up GEMM launch the other 388 rows and expert 2's 100 (a solo tile).
+    sh = _Shape(T=1000, E=4, k=1, H=256, I=128, fat_threshold=32, thin_mma_min=0)
+    counts = np.array([600, 300, 100, 0])
+    w = bench.stage_work(sh, counts)
+    H, I = 256, 128
+    assert w["gather"]["bytes"] == 512 * H * 4
+    assert w["gemm_gate_up"]["bytes"] == (3 * (2 * I * H * 2) + 1000 * (H + I) * 2
+                                          + (1000 - 512) * H * 4)
 
 
 def test_stage_work_self_routed_batch_has_no_gather():

@@ -49,7 +49,7 @@ def _forward(moe, shape, d, profiled=False):
 MMA_ALL, MMA_NONE = 1, 33
 # Widths at which a self-routed batch on the CUDA-core streaming kernel runs
 # the whole layer in one cooperative launch (two launches elsewhere).
-ONE_LAUNCH_WIDTHS = {(4096, 2048), (512, 256)}
+ONE_LAUNCH_WIDTHS = {(4096, 2048), (2048, 1024), (512, 256)}
 
 
 def self_routed_launches(H, I, mma_min):
@@ -164,6 +164,7 @@ SELF_ROUTED = [
     (5, 3, 2, 768, 512),       # sizes that are not powers of two
     (2, 1, 1, 256, 256),       # a single expert
     (6, 8, 5, 1280, 768),      # 30 slots, k = 5
+    (2, 64, 8, 2048, 1024),    # one launch on CUDA cores at this width
 ]
 
 
