@@ -105,6 +105,35 @@ def test_self_routed_decode_wait_expiry(moe, H, I, mma_min, launches):
     assert_close(after, ref, "decode after a timed-out step")
 
 
+def test_planned_batch_fused_combine_wait_expiry(moe):
+    """A planned batch of 8 tokens on the tensor-core streaming kernel alone
+    (router, route lists, gather, gate/up, and a cooperative down launch that
+    waits, bounded, for every CTA before combining) that times out, then
+    normal steps on the same workspace: MOE_ERR_TIMEOUT once, then outputs
+    identical to a step before it and close to the oracle."""
+    B, E, k, H, I = 8, 64, 8, 512, 256
+    Wg, Wu, Wd = synth.make_weights(E, H, I, seed=43, layer=0, device="cuda")
+    shape = moe.Shape(B, E, k, H, I, fat_threshold=32, thin_mma_min=MMA_ALL)
+    assert moe.forward_launches(shape) == 5
+    ws = moe.Workspace(moe.workspace_size(shape))
+    x = synth.make_x(B, H, seed=43)
+    lg = synth.make_logits(B, E, seed=43, zipf_s=synth.ZIPF_S)
+    xd, lgd = x.cuda(), lg.cuda()
+    before = moe.moe_forward(shape, lgd, xd, Wg, Wu, Wd, ws=ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    _timed_out(moe, lambda: moe.moe_forward(shape, lgd, xd, Wg, Wu, Wd, ws=ws))
+    assert ws.status(clear=True) == MOE_ERR_TIMEOUT
+    for _ in range(2):
+        after = moe.moe_forward(shape, lgd, xd, Wg, Wu, Wd, ws=ws)
+        torch.cuda.synchronize()
+        assert ws.status() == 0
+        assert torch.equal(after, before)
+    ref, _, _ = oracle_rows(synth.bf16_bits(x), lg.numpy(), k, DeviceExperts(Wg, Wu, Wd),
+                            np.arange(B))
+    assert_close(after, ref, "planned batch after a timed-out step")
+
+
 def test_wait_limit_argument_checked(moe):
     with pytest.raises(moe.MoeError):
         moe.debug_set_wait_limit(-1)
