@@ -72,16 +72,17 @@ def test_expert_kernel_wait_expiry(moe, case):
         assert torch.equal(after, before), case
 
 
-@pytest.mark.parametrize("H,I,mma_min,launches", [(1024, 512, MMA_NONE, 2),
-                                                  (1024, 512, MMA_ALL, 2),
-                                                  (512, 256, MMA_NONE, 1)])
+@pytest.mark.parametrize("H,I,mma_min,launches", [(1024, 2048, MMA_NONE, 2),
+                                                  (1024, 2048, MMA_ALL, 2),
+                                                  (2048, 1024, MMA_NONE, 1)])
 def test_self_routed_decode_wait_expiry(moe, H, I, mma_min, launches):
     """A decode step routed inside the streaming kernels (two launches, the
-    combine fused into the down kernel; or, at H=512, I=256 on CUDA cores,
+    combine fused into the down kernel; or, at H=2048, I=1024 on CUDA cores,
     the whole layer in one cooperative launch whose down phase also waits,
     bounded, for every CTA's gate/up phase) that times out, then normal steps
     on the same workspace: status MOE_ERR_TIMEOUT once, then correct
-    outputs."""
+    outputs.  The layers are large enough that every CTA's weight ring wraps
+    several times, so its producer must wait for released slots."""
     B, E, k = 2, 64, 8
     Wg, Wu, Wd = synth.make_weights(E, H, I, seed=41, layer=0, device="cuda")
     shape = moe.Shape(B, E, k, H, I, fat_threshold=32, thin_mma_min=mma_min)
