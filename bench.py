@@ -87,7 +87,7 @@ def load_peaks():
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons every 100 ms while
+    """Samples nvidia-smi clocks and throttle reasons every 20 ms while
     running; each sample carries its host time so a timed window can be
     picked out (mark() brackets it)."""
 
@@ -106,7 +106,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
