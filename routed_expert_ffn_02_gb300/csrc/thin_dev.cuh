@@ -194,21 +194,24 @@ struct Range {
 // First item whose cumulative cost reaches c: units have ipe items each, all
 // of cost thin_unit_cost(n); units[u].cost_before is the per-item cost of the
 // units before u.
-__device__ __forceinline__ int item_at(const ThinUnit* units, int n_units, int ipe, int64_t c) {
+template <typename C>   // uint32_t when every cost fits, else int64_t
+__device__ __forceinline__ int item_at(const ThinUnit* units, int n_units, int ipe, C c) {
     int lo = 0, hi = n_units - 1;   // largest u with ipe * cost_before <= c
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if ((int64_t)units[mid].cost_before * ipe <= c) lo = mid;
+        if ((C)units[mid].cost_before * (C)ipe <= c) lo = mid;
         else hi = mid - 1;
     }
-    const int w = thin_unit_cost(units[lo].n);
-    const int64_t off = c - (int64_t)units[lo].cost_before * ipe;
-    const int64_t k = (off + w - 1) / w;
-    return lo * ipe + (int)(k < ipe ? k : ipe);
+    const C w = (C)thin_unit_cost(units[lo].n);
+    const C off = c - (C)units[lo].cost_before * (C)ipe;
+    const C k = (off + w - 1) / w;
+    return lo * ipe + (int)(k < (C)ipe ? k : (C)ipe);
 }
 
 // This CTA's contiguous share of the items of n_units units of total cost
-// `weight` (per item), of (about) equal total cost.
+// `weight` (per item), of (about) equal total cost.  The arithmetic is 32-bit
+// where the products fit (every self-routed batch: it runs before the first
+// weight copy, so its length matters there), 64-bit otherwise.
 __device__ __forceinline__ Range cta_range(const ThinUnit* units, int n_units, int weight, int ipe) {
     Range r;
     if (n_units <= 0) {
@@ -218,11 +221,21 @@ __device__ __forceinline__ Range cta_range(const ThinUnit* units, int n_units, i
         return r;
     }
     const int64_t total = (int64_t)weight * ipe;
-    const int64_t c0 = total * blockIdx.x / gridDim.x;
-    const int64_t c1 = total * (blockIdx.x + 1) / gridDim.x;
-    r.beg = item_at(units, n_units, ipe, c0);
-    const int end = blockIdx.x + 1 == gridDim.x ? n_units * ipe : item_at(units, n_units, ipe, c1);
-    r.cnt = end - r.beg;
+    const bool last = blockIdx.x + 1 == gridDim.x;
+    if (total * gridDim.x < (int64_t)1 << 32) {
+        const uint32_t t = (uint32_t)total;
+        r.beg = item_at<uint32_t>(units, n_units, ipe, t * blockIdx.x / gridDim.x);
+        const int end = last ? n_units * ipe
+                             : item_at<uint32_t>(units, n_units, ipe,
+                                                 t * (blockIdx.x + 1) / gridDim.x);
+        r.cnt = end - r.beg;
+    } else {
+        r.beg = item_at<int64_t>(units, n_units, ipe, total * blockIdx.x / gridDim.x);
+        const int end = last ? n_units * ipe
+                             : item_at<int64_t>(units, n_units, ipe,
+                                                total * (blockIdx.x + 1) / gridDim.x);
+        r.cnt = end - r.beg;
+    }
     r.u_first = r.beg / ipe;
     r.u_last = r.cnt > 0 ? (r.beg + r.cnt - 1) / ipe : r.u_first - 1;
     return r;
