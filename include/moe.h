@@ -241,10 +241,13 @@ int32_t moe_forward_launches(const moe_shape* shape);
 
 /* Expert weights kept in pinned host memory and streamed into a ring of
  * device staging slots on a side copy stream, overlapped with compute, the
- * copy engine running ahead into the next layers (dsv41-flash-offload wiki,
+ * copies running ahead into the next layers (dsv41-flash-offload wiki,
  * overview: experts pinned in host RAM, copied into VRAM slots in batches on
- * the copy engine, 8 staging slots, cross-layer DMA prefetch).  One slot holds
- * one layer's whole expert set. */
+ * the copy engine, 8 staging slots, cross-layer DMA prefetch).  The copies
+ * here are one kernel per layer that reads host memory with SM loads: on a
+ * GB300 with a Grace host it holds the host link at its full rate, where the
+ * copy engine's one copy per run of experts does not.  One slot holds one
+ * layer's whole expert set. */
 typedef struct moe_stager moe_stager;
 
 /* Bytes of one layer's expert set: W_gate | W_up | W_down, bf16, in that
@@ -263,19 +266,22 @@ moe_status moe_stager_destroy(moe_stager* stager);
 
 /* Runs n_layers independent layers on the same activations x [T, H] (device)
  * with logits[l] [T, E] and out[l] [T, H] (device), expert weights in
- * host_weights[l] (pinned host memory, moe_layer_weight_bytes bytes,
+ * host_weights[l] (pinned host memory from cudaHostAlloc or
+ * cudaHostRegister, 16-byte aligned, moe_layer_weight_bytes bytes,
  * W_gate | W_up | W_down).  First every layer is routed on `compute` and the
  * experts it touches are marked in a pinned flag array owned by the stager;
  * the call synchronises `compute` once to read them (wiki file map: only
- * experts with positive counts are copied).  Then, for layer l, each run of
- * consecutive touched experts of each matrix is copied into the same offsets
- * of slot l mod n_slots on `copy`, once the compute that last used that slot
- * has finished, and moe_forward runs on `compute` once the copies have
- * landed; untouched experts' regions of the slot are neither copied nor
- * read.  All copies are enqueued up front, so the copy engine works up to
- * n_slots layers ahead.  `copy` must differ from `compute`; ws as for
- * moe_forward.  Errors as moe_forward, plus MOE_ERR_CUDA if the flag array
- * cannot be allocated. */
+ * experts with positive counts are copied).  Then, for layer l, one copy
+ * kernel on `copy` moves the touched experts' three matrices into the same
+ * offsets of slot l mod n_slots, reading the host memory with SM loads over
+ * the host link, once the compute that last used that slot has finished, and
+ * moe_forward runs on `compute` once the copy has landed; untouched experts'
+ * regions of the slot are neither copied nor read.  All copies are enqueued
+ * up front, so they run up to n_slots layers ahead.  `copy` must differ from
+ * `compute`; ws as for moe_forward.  Errors as moe_forward, plus
+ * MOE_ERR_INVALID_ARG (nothing enqueued) if a host_weights[l] is not 16-byte
+ * aligned pinned host memory and MOE_ERR_CUDA if the flag array cannot be
+ * allocated. */
 moe_status moe_forward_offload(moe_stager* stager, const moe_shape* shape, int32_t n_layers,
                                const float* const* logits, const moe_bf16* x,
                                const void* const* host_weights, moe_bf16* const* out,

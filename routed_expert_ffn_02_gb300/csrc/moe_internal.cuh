@@ -328,6 +328,27 @@ cudaError_t launch_combine(const __nv_bfloat16* y_sorted, const int32_t* inv_per
                            const float* gates, int T, int k, int H,
                            __nv_bfloat16* out, int num_sms, cudaStream_t s);
 
+// Experts to copy: entry j copies expert src_e[j] of the source matrices
+// into block dst_e[j] of the destination matrices.
+struct ExpertCopyList {
+    int32_t n;
+    int32_t src_e[kMaxE];
+    int32_t dst_e[kMaxE];
+};
+
+// The device's pointer to pinned host memory `host` (cudaHostAlloc or
+// cudaHostRegister); cudaErrorInvalidValue for any other memory.
+cudaError_t device_view_of_host(const void* host, const void** dev);
+
+// For each list entry and matrix m < 3: copies expert_bytes from
+// src[m] + src_e * expert_bytes (device-visible host memory, see
+// device_view_of_host) to dst[m] + dst_e * expert_bytes (device), in one
+// kernel whose CTAs drive the host link with SM loads.  Every pointer and
+// expert_bytes must be 16-byte aligned (else cudaErrorInvalidValue, nothing
+// launched).
+cudaError_t launch_expert_copy(const ExpertCopyList& list, const void* const src[3],
+                               void* const dst[3], size_t expert_bytes, cudaStream_t s);
+
 // Routes `logits` into the routing buffers of a moe_forward workspace and
 // sets flags[e] = 1 for each expert the layer touches (asynchronous on s).
 moe_status mark_touched_experts(const moe_shape* shape, const float* logits, void* ws,

@@ -2,10 +2,13 @@
 // staging slots on a side copy stream, overlapped with the layers' compute.
 //
 // All routed experts are kept in pinned host memory and copied into a ring
-// of device staging slots in batches by the copy engine, overlapped with
-// compute, with the next layers' copies issued while the current layer runs
-// (dsv41-flash-offload wiki, overview and its notes on 8 staging slots and
-// cross-layer DMA prefetch).  Here one slot has room for one layer's whole
+// of device staging slots in batches, overlapped with compute, with the next
+// layers' copies issued while the current layer runs (dsv41-flash-offload
+// wiki, overview and its notes on 8 staging slots and cross-layer DMA
+// prefetch).  The wiki's batches go through the copy engine; here one copy
+// kernel per layer moves them with SM loads, which keep the host link at its
+// full rate where the copy engine's many separate copies do not (see
+// expert_copy.cu).  Here one slot has room for one layer's whole
 // expert set (W_gate | W_up | W_down, the layout moe_forward takes), but only
 // the experts the layer's tokens are routed to are copied (the wiki's file
 // map: one weight copy per batch for the experts with positive counts).
@@ -14,15 +17,15 @@
 //      pinned host flag array (written by the GPU); synchronise once.
 //   2. for layer l (slot s = l mod n_slots):
 //      copy stream:    wait for the compute that last used slot s (layer
-//                      l - n), one cudaMemcpyAsync per matrix per run of
-//                      consecutive touched experts into the same offsets of
-//                      slot s, record copied[s]
+//                      l - n), one copy kernel for the touched experts'
+//                      three matrices into the same offsets of slot s,
+//                      record copied[s]
 //      compute stream: wait copied[s], moe_forward on the slot, record
 //                      freed[s]
 //
 // Untouched experts' regions of a slot keep stale bytes and are never read:
 // no token is routed to them.  Every copy for all layers is enqueued up front,
-// so the copy engine runs up to n_slots layers ahead of the compute.  The
+// so the copies run up to n_slots layers ahead of the compute.  The
 // caller owns the slot memory; the stager holds its events and the flag
 // array (pinned host memory, grown on demand).
 #include <cstdlib>
@@ -40,6 +43,7 @@ struct moe_stager {
     uint8_t* flags_h;      // [n_layers x E] touched flags, pinned and mapped
     uint8_t* flags_d;      // the device's view of flags_h
     size_t flags_cap;
+    moe::ExpertCopyList list;   // the layer being enqueued
 };
 
 namespace {
@@ -130,9 +134,16 @@ extern "C" moe_status moe_forward_offload(moe_stager* st, const moe_shape* shape
     const int E = shape->E;
     const size_t per = (size_t)E * shape->I * shape->H;            // elements per matrix
     const size_t per_expert = (size_t)shape->I * shape->H * sizeof(moe_bf16);
-    for (int l = 0; l < n_layers; ++l)
+    for (int l = 0; l < n_layers; ++l) {
         if (!host_weights[l] || !logits[l] || !out[l])
             return stager_fail(MOE_ERR_INVALID_ARG, "moe_forward_offload: NULL layer pointer");
+        const void* view = nullptr;
+        if (moe::device_view_of_host(host_weights[l], &view) != cudaSuccess ||
+            reinterpret_cast<uintptr_t>(view) % 16)
+            return stager_fail(MOE_ERR_INVALID_ARG,
+                               "moe_forward_offload: host weights must be 16-byte aligned pinned "
+                               "host memory");
+    }
     if (n_layers == 0 || shape->T == 0) {
         moe::set_last_error("");
         return MOE_OK;
@@ -172,25 +183,24 @@ extern "C" moe_status moe_forward_offload(moe_stager* st, const moe_shape* shape
     for (int l = 0; l < n_layers; ++l) {
         const int s = l % st->n_slots;
         uint8_t* slot = st->slots + (size_t)s * st->slot_bytes;
-        const uint8_t* src = static_cast<const uint8_t*>(host_weights[l]);
         const uint8_t* touched = st->flags_h + (size_t)l * E;
+        st->list.n = 0;
+        for (int x = 0; x < E; ++x)
+            if (touched[x]) {
+                st->list.src_e[st->list.n] = x;
+                st->list.dst_e[st->list.n] = x;
+                ++st->list.n;
+            }
+        const void* src = nullptr;
+        if (e == cudaSuccess) e = moe::device_view_of_host(host_weights[l], &src);   // checked above
+        const size_t mat = per * sizeof(moe_bf16);
+        const void* srcs[3] = {src, static_cast<const uint8_t*>(src) + mat,
+                               static_cast<const uint8_t*>(src) + 2 * mat};
+        void* dsts[3] = {slot, slot + mat, slot + 2 * mat};
         // The slot may be refilled only once the compute of its last layer
         // has finished (that event was recorded in an earlier iteration).
-        if (l >= st->n_slots) e = cudaStreamWaitEvent(ks, st->freed[s], 0);
-        for (int e0 = 0; e == cudaSuccess && e0 < E;) {
-            if (!touched[e0]) {
-                ++e0;
-                continue;
-            }
-            int e1 = e0 + 1;
-            while (e1 < E && touched[e1]) ++e1;
-            const size_t off = (size_t)e0 * per_expert, len = (size_t)(e1 - e0) * per_expert;
-            for (int m = 0; e == cudaSuccess && m < 3; ++m) {
-                const size_t mo = (size_t)m * per * sizeof(moe_bf16) + off;
-                e = cudaMemcpyAsync(slot + mo, src + mo, len, cudaMemcpyHostToDevice, ks);
-            }
-            e0 = e1;
-        }
+        if (e == cudaSuccess && l >= st->n_slots) e = cudaStreamWaitEvent(ks, st->freed[s], 0);
+        if (e == cudaSuccess) e = moe::launch_expert_copy(st->list, srcs, dsts, per_expert, ks);
         if (e == cudaSuccess) e = cudaEventRecord(st->copied[s], ks);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, st->copied[s], 0);
         if (e != cudaSuccess) {

@@ -85,4 +85,11 @@ def test_offload_argument_errors(moe):
         st.forward(small, [torch.zeros((8, 8), device="cuda")], x,
                    [torch.zeros(moe.layer_weight_bytes(small) // 2, dtype=torch.bfloat16).pin_memory()],
                    compute=s2, copy=s2)          # copy stream must differ
+    nbytes = moe.layer_weight_bytes(small)
+    pageable = torch.zeros(nbytes // 2, dtype=torch.bfloat16)
+    with pytest.raises(moe.MoeError, match="pinned"):
+        st.forward(small, [torch.zeros((8, 8), device="cuda")], x, [pageable])
+    pinned = torch.zeros(nbytes // 2 + 8, dtype=torch.bfloat16).pin_memory()
+    with pytest.raises(moe.MoeError, match="16-byte aligned"):
+        st.forward(small, [torch.zeros((8, 8), device="cuda")], x, [pinned[1:1 + nbytes // 2]])
     st.close()
