@@ -315,17 +315,21 @@ moe_status moe_cache_stats(const moe_cache* cache, int64_t* hits, int64_t* misse
 
 /* Runs n_layers independent layers on x [T, H] (device) with logits[l]
  * [T, E] and out[l] [T, H] (device); layer l's experts are host_weights[l]
- * (pinned host memory, W_gate | W_up | W_down as for moe_forward_offload),
- * cached under the key (layer_ids[l], expert), layer_ids[l] >= 0.  First every
- * layer is routed on `compute` and its touched experts marked in pinned host
- * flags; the call synchronises `compute` once to read them.  Then, per layer:
- * each touched expert not resident is copied on `copy` into the least
- * recently used slot that layer l does not need, once the compute of the
- * last layer that read the slot has finished; the layer runs on `compute`
- * once its copies have landed.  n_layers <= max_layers; every layer must
- * touch at most n_slots experts (else MOE_ERR_INVALID_ARG, with the earlier
- * layers already enqueued).  `copy` must differ from `compute`; ws as for
- * moe_forward.  Errors as moe_forward. */
+ * (16-byte aligned pinned host memory, W_gate | W_up | W_down as for
+ * moe_forward_offload), cached under the key (layer_ids[l], expert),
+ * layer_ids[l] >= 0.  First every layer is routed on `compute` and its
+ * touched experts marked in pinned host flags; the call synchronises
+ * `compute` once to read them.  Then, per layer: each touched expert not
+ * resident is assigned the least recently used slot that layer l does not
+ * need, and one copy kernel on `copy` moves the layer's misses in (SM loads
+ * over the host link, as in moe_forward_offload) once the compute of the
+ * last layers that read those slots has finished; the layer runs on
+ * `compute` once its copies have landed.  n_layers <= max_layers; every
+ * layer must touch at most n_slots experts (else MOE_ERR_INVALID_ARG, with
+ * the earlier layers already enqueued).  `copy` must differ from `compute`;
+ * ws as for moe_forward.  Errors as moe_forward, plus MOE_ERR_INVALID_ARG
+ * (nothing enqueued) for host weights that are not 16-byte aligned pinned
+ * host memory. */
 moe_status moe_forward_cached(moe_cache* cache, const moe_shape* shape, int32_t n_layers,
                               const int32_t* layer_ids, const float* const* logits,
                               const moe_bf16* x, const void* const* host_weights,

@@ -13,7 +13,9 @@
 //   2. for layer l: each touched expert is a hit (already in a slot) or a
 //      miss; a miss takes the least recently used slot not needed by layer l
 //      and is copied in on the copy stream (W_gate, W_up, W_down rows of that
-//      expert), after the compute of the last layer that read the slot.  The
+//      expert), after the compute of the last layer that read the slot; one
+//      copy kernel per layer moves all of its misses (SM loads over the host
+//      link, see expert_copy.cu).  The
 //      layer's expert -> slot table goes to the device on the compute stream,
 //      which waits for the layer's copies and runs the layer on the slots.
 //
@@ -56,6 +58,7 @@ struct moe_cache {
     int32_t* tables_h;           // pinned staging of the same
     uint8_t* flags_h = nullptr;  // [max_layers, E] touched flags, pinned and mapped
     uint8_t* flags_d = nullptr;
+    moe::ExpertCopyList list;         // the misses of the layer being enqueued
     std::vector<int64_t> key;         // per slot: layer_id << 32 | expert, -1 when empty
     std::vector<int64_t> last_use;    // per slot: tick of the last layer that needed it
     std::vector<int> reader;          // per slot: done[] index of that layer, -1 if none
@@ -154,9 +157,16 @@ extern "C" moe_status moe_forward_cached(moe_cache* c, const moe_shape* shape, i
     if (compute == copy)
         return cache_fail(MOE_ERR_INVALID_ARG,
                           "moe_forward_cached: the copy stream must differ from the compute stream");
-    for (int l = 0; l < n_layers; ++l)
+    for (int l = 0; l < n_layers; ++l) {
         if (layer_ids[l] < 0 || !logits[l] || !host_weights[l] || !out[l])
             return cache_fail(MOE_ERR_INVALID_ARG, "moe_forward_cached: bad layer pointer or id");
+        const void* view = nullptr;
+        if (moe::device_view_of_host(host_weights[l], &view) != cudaSuccess ||
+            reinterpret_cast<uintptr_t>(view) % 16)
+            return cache_fail(MOE_ERR_INVALID_ARG,
+                              "moe_forward_cached: host weights must be 16-byte aligned pinned "
+                              "host memory");
+    }
     if (n_layers == 0 || shape->T == 0) {
         moe::set_last_error("");
         return MOE_OK;
@@ -204,7 +214,7 @@ extern "C" moe_status moe_forward_cached(moe_cache* c, const moe_shape* shape, i
                 miss.push_back(ex);
             }
         }
-        const uint8_t* src = static_cast<const uint8_t*>(host_weights[l]);
+        c->list.n = 0;
         for (int ex : miss) {
             int victim = -1;
             for (int s = 0; s < c->n_slots; ++s)
@@ -215,12 +225,9 @@ extern "C" moe_status moe_forward_cached(moe_cache* c, const moe_shape* shape, i
             if (c->reader[victim] >= 0 &&
                 (e = cudaStreamWaitEvent(ks, c->done[c->reader[victim]], 0)) != cudaSuccess)
                 return cuda_fail("moe_forward_cached", e);
-            const size_t so = (size_t)victim * eb, eo = (size_t)ex * eb;
-            const size_t mat = (size_t)E * eb;   // bytes of one matrix for all experts
-            if ((e = cudaMemcpyAsync(c->wg + so, src + eo, eb, cudaMemcpyHostToDevice, ks)) != cudaSuccess ||
-                (e = cudaMemcpyAsync(c->wu + so, src + mat + eo, eb, cudaMemcpyHostToDevice, ks)) != cudaSuccess ||
-                (e = cudaMemcpyAsync(c->wd + so, src + 2 * mat + eo, eb, cudaMemcpyHostToDevice, ks)) != cudaSuccess)
-                return cuda_fail("moe_forward_cached", e);
+            c->list.src_e[c->list.n] = ex;
+            c->list.dst_e[c->list.n] = victim;
+            ++c->list.n;
             const int64_t k = ((int64_t)layer_ids[l] << 32) | (uint32_t)ex;
             c->key[victim] = k;
             c->where[k] = victim;
@@ -229,6 +236,15 @@ extern "C" moe_status moe_forward_cached(moe_cache* c, const moe_shape* shape, i
             table[ex] = victim;
             ++c->misses;
         }
+        const void* src = nullptr;
+        if ((e = moe::device_view_of_host(host_weights[l], &src)) != cudaSuccess)   // checked above
+            return cuda_fail("moe_forward_cached", e);
+        const size_t mat = (size_t)E * eb;   // bytes of one matrix for all experts
+        const void* srcs[3] = {src, static_cast<const uint8_t*>(src) + mat,
+                               static_cast<const uint8_t*>(src) + 2 * mat};
+        void* dsts[3] = {c->wg, c->wu, c->wd};
+        if ((e = moe::launch_expert_copy(c->list, srcs, dsts, eb, ks)) != cudaSuccess)
+            return cuda_fail("moe_forward_cached", e);
         int32_t* table_d = c->tables_d + (size_t)l * E;
         if ((e = cudaEventRecord(c->copied[ev], ks)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(cs, c->copied[ev], 0)) != cudaSuccess ||

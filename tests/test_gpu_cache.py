@@ -98,3 +98,23 @@ def test_cache_too_small_for_a_layer(moe):
     assert ei.value.status == 1
     torch.cuda.synchronize()
     cache.close()
+
+
+def test_cache_rejects_host_weights_it_cannot_read(moe):
+    """The misses are copied by a kernel that reads host memory through the
+    device's mapping: pageable or misaligned host weights are refused before
+    anything is enqueued."""
+    T, E, k, H, I = 8, 16, 2, 512, 256
+    dev = torch.device("cuda")
+    shape = moe.Shape(T, E, k, H, I)
+    cache = moe.ExpertCache(shape, E, 1)
+    x = synth.make_x(T, H, seed=8).to(dev)
+    logits = [synth.make_logits(T, E, seed=31).to(dev)]
+    n = moe.layer_weight_bytes(shape) // 2
+    with pytest.raises(moe.MoeError, match="pinned"):
+        cache.forward([0], logits, x, [torch.zeros(n, dtype=torch.bfloat16)])
+    pinned = torch.zeros(n + 8, dtype=torch.bfloat16).pin_memory()
+    with pytest.raises(moe.MoeError, match="16-byte aligned"):
+        cache.forward([0], logits, x, [pinned[1:1 + n]])
+    assert cache.stats() == (0, 0)
+    cache.close()
