@@ -20,7 +20,8 @@ def moe():
 @pytest.mark.parametrize("T,E,k,H,I,L,slots", [(64, 16, 2, 512, 256, 4, 1),
                                                 (64, 16, 2, 512, 256, 5, 2),
                                                 (1024, 32, 8, 2048, 1024, 4, 3),
-                                                (4, 64, 8, 2048, 1024, 3, 8)])
+                                                (4, 64, 8, 2048, 1024, 3, 8),
+                                                (512, 1024, 8, 256, 256, 2, 2)])
 def test_offload_matches_resident_forward(moe, T, E, k, H, I, L, slots):
     s = synth.Shape(T=T, E=E, k=k, H=H, I=I)
     shape = moe.Shape(T, E, k, H, I)
