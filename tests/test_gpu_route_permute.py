@@ -30,6 +30,10 @@ ROUTE_CASES = [  # (T, E, k, zipf)
     (64, 16, 2, None), (1, 384, 8, 1.1), (4, 384, 8, 1.1), (24, 384, 8, 1.1),
     (16384, 384, 8, 1.1), (100, 1, 1, None), (77, 3, 3, None), (50, 33, 5, None),
     (300, 1024, 8, 1.1), (40, 100, 7, None), (513, 32, 8, None), (9, 64, 1, None),
+    # batches of prefill size at every k, E a multiple of 4 or not
+    (4096, 384, 8, 1.1), (5000, 1024, 8, 1.1), (4099, 100, 3, None), (4161, 4, 4, None),
+    (6000, 132, 1, None), (4500, 64, 2, 1.1), (4100, 256, 5, None), (4127, 20, 6, None),
+    (4096, 512, 7, 1.1), (4096, 33, 5, None), (5000, 7, 7, None),
 ]
 
 
@@ -49,6 +53,34 @@ def test_route_ties_and_special_values(moe):
     _route_check(moe, lg, 2)
     # all experts selected
     _route_check(moe, synth.make_logits(33, 8, seed=3), 8)
+
+
+def test_route_ties_and_special_values_large_batch(moe):
+    """The same cases in batches of prefill size."""
+    _route_check(moe, synth.tied_logits(5000, 64, seed=4, levels=3), 8)
+    lg = synth.tied_logits(4200, 40, seed=5, levels=2)
+    lg[:, 5::3] = -float("inf")
+    _route_check(moe, lg, 8)
+    lg = torch.tensor([[-0.0, 0.0, -1.0, 0.0], [0.0, -0.0, -0.0, -2.0]], dtype=torch.float32)
+    _route_check(moe, lg.repeat(2100, 1), 2)
+    _route_check(moe, synth.make_logits(4100, 8, seed=6), 8)
+
+
+def test_route_independent_of_placement_and_batch(moe):
+    """A token's routing does not depend on where the logits start in
+    memory (4 bytes past a 16-byte boundary here) nor on the batch it is
+    routed in: bit-identical indices and gates."""
+    T, E, k = 4500, 384, 8
+    lg = synth.make_logits(T, E, seed=12, zipf_s=1.1)
+    buf = torch.empty(T * E + 1, dtype=torch.float32, device="cuda")
+    buf[1:].copy_(lg.reshape(-1).cuda())
+    skew = buf[1:].view(T, E)                   # 4 bytes past a 16-byte boundary
+    idx_a, g_a = moe.moe_route(lg.cuda(), k)
+    idx_b, g_b = moe.moe_route(skew, k)
+    idx_c, g_c = moe.moe_route(lg[:40].cuda(), k)
+    torch.cuda.synchronize()
+    assert torch.equal(idx_a, idx_b) and torch.equal(g_a, g_b)
+    assert torch.equal(idx_a[:40], idx_c) and torch.equal(g_a[:40], g_c)
 
 
 def _permute_check(moe, idx_cpu, E):
