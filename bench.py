@@ -309,10 +309,10 @@ def time_steps(layer, steps, warmup, profiled=True, rotate=True, clk=None):
     return total_ms, stage_ms
 
 
-def time_graph_steps(layer, steps, warmup, n_graphs=8):
+def time_graph_steps(layer, steps, warmup, n_graphs=8, clk=None):
     """Times `steps` decode steps replayed through the library's DecodeGraph
     (one captured step per logits set, its static inputs filled once);
-    returns total ms."""
+    returns total ms.  clk: a running ClockSampler, told the timed window."""
     moe = layer.moe
     graphs = []
     for i in range(n_graphs):
@@ -327,11 +327,14 @@ def time_graph_steps(layer, steps, warmup, n_graphs=8):
     end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     barrier()
+    t0 = time.monotonic()
     start.record()
     for i in range(steps):
         graphs[i % n_graphs].replay()
     end.record()
     torch.cuda.synchronize()
+    if clk is not None:
+        clk.mark(t0, time.monotonic())
     barrier()
     for g in graphs:
         assert g.ws.status() == 0
@@ -781,9 +784,13 @@ def run_gpu(args):
             dl = Layer(moe, dshape, dev, n_logit_sets=8, weights=(layer.Wg, layer.Wu, layer.Wd))
             dcounts = dl.counts()
             dwork = stage_work(dshape, dcounts)
-            reps = max(args.steps, 50)
-            dt, dst = time_steps(dl, reps, max(args.warmup, 5))
-            gt = time_graph_steps(dl, reps, max(args.warmup, 5))
+            # a few hundred replays (tens of ms) so that the clock sampler
+            # sees the timed window
+            reps = max(args.steps, 500)
+            with ClockSampler(local) as dclk:
+                dt, dst = time_steps(dl, reps, max(args.warmup, 5))
+                gt = time_graph_steps(dl, reps, max(args.warmup, 5), clk=dclk)
+            dclocks = dclk.summary()
             dt, gt = max_over_ranks(dt), max_over_ranks(gt)
             bytes_step = sum(w["bytes"] for n, w in dwork.items() if not n.startswith("_"))
             decode[f"B{B}"] = {
@@ -796,6 +803,9 @@ def run_gpu(args):
                 "layer_frac_of_nominal_hbm": round(
                     bytes_step / (gt / reps * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
                 "stage_us_eager": {s: round(1e3 * v, 2) for s, v in dst.items()},
+                "clocks": {"sm_mhz": dclocks.get("sm_mhz"), "samples": dclocks.get("samples"),
+                           "reasons": dclocks.get("reasons"),
+                           "leg_sm_mhz_min": dclocks.get("run", {}).get("sm_mhz_min")},
             }
             del dl
 
