@@ -75,10 +75,10 @@ thin_gate_up_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
     }
 
     const bool ok = consume<16>(m, rg, ipe, U, warp - kProducers, nc, wait_cycles,
-                                [&]<int N>(int it, int slot) {
+                                [&]<int N>(int it, int slot, const Smem& mu) {
         const ThinUnit un = U[it / ipe];
         __nv_bfloat16* hcol = h + (int64_t)un.row0 * I + (it % ipe) * R;
-        gate_up_slot<N, VPL>(m, slot, R, vec, un.n, hcol, I);
+        gate_up_slot<N, VPL>(mu, slot, R, vec, un.n, hcol, I);
     });
     if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
 }

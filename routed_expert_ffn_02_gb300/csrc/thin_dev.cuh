@@ -142,44 +142,59 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 
 // ---- shared-memory layout and pipeline ------------------------------------
 
-// [slots x stage_bytes weight ring][activation buffer][barriers]
+// [slots x stage_bytes weight ring][activation buffers][barriers]
 // Each producer's copies into a slot complete on its own full barrier
 // (full(s) for producer 0, full2(s) for producer 1), so a producer that
-// stops early can still wait for exactly the copies it issued.
-constexpr int kBarriers = 3 * kMaxSlots + 2;
+// stops early can still wait for exactly the copies it issued.  With two
+// activation buffers, unit i of a range is staged in buffer i % 2, so the
+// next unit's rows arrive while the current one is consumed.
+constexpr int kBarriers = 3 * kMaxSlots + 4;
 struct Smem {
     uint32_t base;       // shared addresses
-    uint32_t act;
+    uint32_t act;        // the activation buffer the consumers read
     uint32_t bars;
+    uint32_t act_bytes;  // per buffer
+    int act_bufs;
     int stage_bytes;
     int slots;
     int producers;
     __device__ uint32_t buf(int s) const { return base + (uint32_t)(s * stage_bytes); }
     __device__ uint32_t full(int s) const { return bars + 8u * s; }
     __device__ uint32_t empty(int s) const { return bars + 8u * (kMaxSlots + s); }
-    __device__ uint32_t act_full() const { return bars + 8u * (2 * kMaxSlots); }
-    __device__ uint32_t act_free() const { return bars + 8u * (2 * kMaxSlots + 1); }
+    __device__ uint32_t act_buf(int b) const { return act + (uint32_t)b * act_bytes; }
+    __device__ uint32_t act_full(int b = 0) const {
+        return bars + 8u * (b == 0 ? 2 * kMaxSlots : 3 * kMaxSlots + 2);
+    }
+    __device__ uint32_t act_free(int b = 0) const {
+        return bars + 8u * (b == 0 ? 2 * kMaxSlots + 1 : 3 * kMaxSlots + 3);
+    }
     __device__ uint32_t full2(int s) const { return bars + 8u * (2 * kMaxSlots + 2 + s); }
     // full barrier of producer p
     __device__ uint32_t full_of(int p, int s) const { return p == 0 ? full(s) : full2(s); }
 };
 
+// act_bytes: one activation buffer; act_bufs: 1 or 2 buffers.
 __device__ __forceinline__ Smem smem_setup(uint8_t* smem, int stage_bytes, int slots,
-                                           int act_bytes, int producers, int consumers) {
+                                           int act_bytes, int producers, int consumers,
+                                           int act_bufs = 1) {
     Smem m;
     m.base = smem_u32(smem);
     m.stage_bytes = stage_bytes;
     m.slots = slots;
     m.producers = producers;
     m.act = m.base + (uint32_t)(slots * stage_bytes);
-    m.bars = m.act + (uint32_t)act_bytes;
+    m.act_bytes = (uint32_t)act_bytes;
+    m.act_bufs = act_bufs;
+    m.bars = m.act + (uint32_t)(act_bytes * act_bufs);
     if (threadIdx.x == 0) {
         for (int s = 0; s < slots; ++s) {
             for (int p = 0; p < producers; ++p) mbar_init(m.full_of(p, s), 1);
             mbar_init(m.empty(s), 1);
         }
-        mbar_init(m.act_full(), 1);
-        mbar_init(m.act_free(), consumers);
+        for (int b = 0; b < act_bufs; ++b) {
+            mbar_init(m.act_full(b), 1);
+            mbar_init(m.act_free(b), consumers);
+        }
         fence_mbar_init();
     }
     __syncthreads();
@@ -250,12 +265,13 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, long lo
 
 // Producer (one lane): streams the range's items through the weight ring
 // (copy_item) and, if it is the `stager`, stages each unit's activations
-// (copy_act) once the consumers have released the previous unit's.  Items
+// (copy_act) into buffer i % kBufs (i: the unit's place in the range) once
+// the consumers have released the unit that used that buffer before.  Items
 // [0, pre) (pre <= slots) were already issued into slots [0, pre).  While a
 // slot is still in use the lane sleeps in try_wait.  Each wait gives up after
 // `limit` cycles; then the copies already issued are waited for (full bound)
 // and it returns false.
-template <typename ItemFn, typename ActFn>
+template <int kBufs = 1, typename ItemFn, typename ActFn>
 __device__ bool produce(const Smem& m, int producer, const Range& rg, bool stager,
                         ItemFn copy_item, ActFn copy_act, long long limit, int pre = 0) {
     if (rg.cnt <= 0) return true;
@@ -263,16 +279,19 @@ __device__ bool produce(const Smem& m, int producer, const Range& rg, bool stage
     for (int s = 0; s < kMaxSlots; ++s) last_round[s] = s < pre ? 0 : -1;
     const int n_units = stager ? rg.u_last - rg.u_first + 1 : 0;
     int act_issued = 0;                       // units whose activations are staged
-    if (stager) {
-        copy_act(rg.u_first, m.act, m.act_full());
-        act_issued = 1;
-    }
+    for (; act_issued < kBufs && act_issued < n_units; ++act_issued)
+        copy_act(rg.u_first + act_issued, m.act_buf(act_issued), m.act_full(act_issued));
+    // Unit i goes to buffer i % kBufs once the release of unit i - kBufs
+    // (that buffer's use number i / kBufs - 1) has completed.
+    auto stage_next = [&]() {
+        const int b = act_issued % kBufs;
+        copy_act(rg.u_first + act_issued, m.act_buf(b), m.act_full(b));
+        ++act_issued;
+    };
+    auto freed_parity = [&]() { return (uint32_t)((act_issued / kBufs - 1) & 1); };
     auto try_stage = [&]() {   // never blocks
-        if (act_issued < n_units &&
-            mbar_test_wait(m.act_free(), (uint32_t)((act_issued - 1) & 1))) {
-            copy_act(rg.u_first + act_issued, m.act, m.act_full());
-            ++act_issued;
-        }
+        if (act_issued < n_units && mbar_test_wait(m.act_free(act_issued % kBufs), freed_parity()))
+            stage_next();
     };
     bool ok = true;
     int slot = pre % m.slots, round = pre / m.slots;
@@ -298,19 +317,21 @@ __device__ bool produce(const Smem& m, int producer, const Range& rg, bool stage
         }
     }
     while (ok && act_issued < n_units) {
-        if (!mbar_wait_for(m.act_free(), (uint32_t)((act_issued - 1) & 1), limit, nullptr)) {
+        if (!mbar_wait_for(m.act_free(act_issued % kBufs), freed_parity(), limit, nullptr)) {
             ok = false;
             break;
         }
-        copy_act(rg.u_first + act_issued, m.act, m.act_full());
-        ++act_issued;
+        stage_next();
     }
     if (!ok) {
         // Let the copies already issued land before the CTA exits.
         for (int s = 0; s < m.slots; ++s)
             if (last_round[s] >= 0)
                 (void)mbar_wait(m.full_of(producer, s), (uint32_t)(last_round[s] & 1));
-        if (act_issued > 0) (void)mbar_wait(m.act_full(), (uint32_t)((act_issued - 1) & 1));
+        for (int b = 0; b < kBufs; ++b) {
+            const int uses = (act_issued - b + kBufs - 1) / kBufs;   // units staged in b
+            if (uses > 0) (void)mbar_wait(m.act_full(b), (uint32_t)((uses - 1) & 1));
+        }
     }
     return ok;
 }
@@ -351,17 +372,22 @@ __device__ __forceinline__ void with_slots(int n, F&& f) {
     }
 }
 
-// Consumer warp c of nc.  For each unit of the range: wait for its
-// activations, then for the warp's items of that unit (seq = c mod nc) wait
-// for the slot and run item.template operator()<N>(item, slot) with N the
-// unit's slot count (the item releases the slot), then release the
-// activations.  Returns false when a wait ran past `limit` cycles.
-template <int kExact, typename ItemFn>
+// Consumer warp c of nc.  For each unit of the range (the i-th, in buffer
+// i % kBufs): wait for its activations, then for the warp's items of that
+// unit (seq = c mod nc) wait for the slot and run
+// item.template operator()<N>(item, slot, mu) with N the unit's slot count
+// and mu the ring with its act pointing at the unit's buffer (the item
+// releases the slot), then release the activations.  Returns false when a
+// wait ran past `limit` cycles.
+template <int kExact, int kBufs = 1, typename ItemFn>
 __device__ bool consume(const Smem& m, const Range& rg, int ipe, const ThinUnit* units, int c,
                         int nc, long long limit, ItemFn item) {
     const int lane = threadIdx.x & 31;
     for (int u = rg.u_first; u <= rg.u_last; ++u) {
-        if (!warp_wait(m.act_full(), (uint32_t)((u - rg.u_first) & 1), limit)) return false;
+        const int i = u - rg.u_first, b = i % kBufs;
+        if (!warp_wait(m.act_full(b), (uint32_t)((i / kBufs) & 1), limit)) return false;
+        Smem mu = m;
+        mu.act = m.act_buf(b);
         const int s0 = max(u * ipe, rg.beg) - rg.beg;
         const int s1 = min((u + 1) * ipe, rg.beg + rg.cnt) - rg.beg;
         const int first = s0 + ((c - s0 % nc) + nc) % nc;
@@ -378,7 +404,7 @@ __device__ bool consume(const Smem& m, const Range& rg, int ipe, const ThinUnit*
                     ok = false;
                     return;
                 }
-                item.template operator()<N>(rg.beg + seq, slot);
+                item.template operator()<N>(rg.beg + seq, slot, mu);
                 slot += nc;            // nc < slots: at most one wrap
                 if (slot >= m.slots) {
                     slot -= m.slots;
@@ -388,7 +414,7 @@ __device__ bool consume(const Smem& m, const Range& rg, int ipe, const ThinUnit*
         });
         if (!ok) return false;
         __syncwarp();
-        if (lane == 0) mbar_arrive(m.act_free());
+        if (lane == 0) mbar_arrive(m.act_free(b));
     }
     return true;
 }
@@ -638,8 +664,10 @@ __device__ __forceinline__ void smem_teardown(const Smem& m) {
             for (int p = 0; p < m.producers; ++p) mbar_inval(m.full_of(p, s));
             mbar_inval(m.empty(s));
         }
-        mbar_inval(m.act_full());
-        mbar_inval(m.act_free());
+        for (int b = 0; b < m.act_bufs; ++b) {
+            mbar_inval(m.act_full(b));
+            mbar_inval(m.act_free(b));
+        }
     }
 }
 
@@ -658,16 +686,17 @@ struct Geometry {
 // act_tokens: most slots any unit can hold here (the activation buffer size);
 // pad4: round the buffer up to a multiple of 4 rows (the down kernel's
 // grouped register path reads whole groups of 4; gate/up reads exactly the
-// unit's rows).  Every H, I the library accepts fits kSmemBudget.
-Geometry geometry(int row_bytes, int act_row_bytes, int act_tokens, bool pad4) {
+// unit's rows); bufs: activation buffers (act is one buffer's bytes).  Every
+// H, I the library accepts fits kSmemBudget.
+Geometry geometry(int row_bytes, int act_row_bytes, int act_tokens, bool pad4, int bufs = 1) {
     Geometry g;
     g.R = rows_per_item(row_bytes);
     g.stage = g.R * row_bytes;
     g.act = (pad4 ? (act_tokens + 3) / 4 * 4 : act_tokens) * act_row_bytes;
-    g.slots = (kSmemBudget - g.act) / g.stage;
+    g.slots = (kSmemBudget - bufs * g.act) / g.stage;
     if (g.slots > kMaxSlots) g.slots = kMaxSlots;
     if (g.slots < 2) g.slots = 2;
-    g.smem = g.slots * g.stage + g.act + 8 * kBarriers;
+    g.smem = g.slots * g.stage + bufs * g.act + 8 * kBarriers;
     return g;
 }
 

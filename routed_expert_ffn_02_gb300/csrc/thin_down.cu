@@ -78,10 +78,10 @@ thin_down_kernel(const __nv_bfloat16* __restrict__ h, int H, int I, int R,
         constexpr int kExact =
             (VPL > 0 && DownRegSlots<VPL>::value > 0) ? DownRegSlots<VPL>::value : 16;
         const bool ok = consume<kExact>(m, rg, ipe, U, warp - kProducers, nc, wait_cycles,
-                                        [&]<int N>(int it, int slot) {
+                                        [&]<int N>(int it, int slot, const Smem& mu) {
             const ThinUnit un = U[it / ipe];
             __nv_bfloat16* ycol = y + (int64_t)un.row0 * H + (it % ipe) * R;
-            down_slot<N, VPL>(m, slot, R, vec, un.n, ycol, H);
+            down_slot<N, VPL>(mu, slot, R, vec, un.n, ycol, H);
         });
         if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
     }

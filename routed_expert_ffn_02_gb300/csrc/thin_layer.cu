@@ -23,7 +23,10 @@ namespace {
 // finish theirs.  VG / VD: the register-cached row paths of the two kernels.
 constexpr int kPreIssueOneToken = 4;
 
-template <int VG, int VD>
+// kBufs: activation buffers of the two rings (2 from two tokens on: a CTA
+// whose range reaches into the next unit has that unit's rows staged while
+// it finishes the current one; a single token keeps one buffer).
+template <int VG, int VD, int kBufs>
 __global__ void __launch_bounds__(kThreads, 1)
 thin_layer_kernel(const __nv_bfloat16* __restrict__ x, int k, int H, int I, int Rg, int Rd,
                   const __nv_bfloat16* __restrict__ Wg, const __nv_bfloat16* __restrict__ Wu,
@@ -41,7 +44,7 @@ thin_layer_kernel(const __nv_bfloat16* __restrict__ x, int k, int H, int I, int 
     {   // ---------------- gate/up ----------------
         constexpr int kProducers = 2;   // warp 0 issues the gate rows, warp 1 the up rows
         const int nc = min(n_warps - kProducers, slots_g - 1);
-        const Smem m = smem_setup(smem, stage_g, slots_g, act_g, kProducers, nc);
+        const Smem m = smem_setup(smem, stage_g, slots_g, act_g, kProducers, nc, kBufs);
         grid_dep_wait();      // the logits may come from the previous kernel
         grid_dep_launch();
         build_small_plan(sr, sp);
@@ -55,7 +58,7 @@ thin_layer_kernel(const __nv_bfloat16* __restrict__ x, int k, int H, int I, int 
                 const uint64_t policy = policy_evict_first();
                 const __nv_bfloat16* W = warp == 0 ? Wg : Wu;
                 const uint32_t part = warp == 0 ? 0u : half;
-                ok = produce(
+                ok = produce<kBufs>(
                     m, warp, rg, warp == 0,
                     [&](int it, uint32_t dst, uint32_t bar) {
                         const ThinUnit un = sp.units[it / ipe];
@@ -74,11 +77,11 @@ thin_layer_kernel(const __nv_bfloat16* __restrict__ x, int k, int H, int I, int 
                     wait_cycles);
             }
         } else if (warp - kProducers < nc) {
-            ok = consume<16>(m, rg, ipe, sp.units, warp - kProducers, nc, wait_cycles,
-                             [&]<int N>(int it, int slot) {
+            ok = consume<16, kBufs>(m, rg, ipe, sp.units, warp - kProducers, nc, wait_cycles,
+                                    [&]<int N>(int it, int slot, const Smem& mu) {
                 const ThinUnit un = sp.units[it / ipe];
                 __nv_bfloat16* hcol = h + (int64_t)un.row0 * I + (it % ipe) * Rg;
-                gate_up_slot<N, VG>(m, slot, Rg, vec, un.n, hcol, I);
+                gate_up_slot<N, VG>(mu, slot, Rg, vec, un.n, hcol, I);
             });
         }
         if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
@@ -97,7 +100,7 @@ thin_layer_kernel(const __nv_bfloat16* __restrict__ x, int k, int H, int I, int 
     if (!failed) {   // ---------------- down ----------------
         constexpr int kProducers = 1;
         const int nc = min(n_warps - kProducers, slots_d - 1);
-        const Smem m = smem_setup(smem, stage_d, slots_d, act_d, kProducers, nc);
+        const Smem m = smem_setup(smem, stage_d, slots_d, act_d, kProducers, nc, kBufs);
         const int vec = I / 8, ipe = H / Rd;
         const Range rg = cta_range(sp.units, sp.n_units, sp.weight, ipe);
         const uint32_t bytes = (uint32_t)Rd * I * 2, hrow = (uint32_t)I * 2;
@@ -130,7 +133,7 @@ thin_layer_kernel(const __nv_bfloat16* __restrict__ x, int k, int H, int I, int 
                     __nanosleep(32);
                 }
                 fence_proxy_async_global();
-                ok = produce(
+                ok = produce<kBufs>(
                     m, 0, rg, true, copy_item,
                     [&](int u, uint32_t dst, uint32_t bar) {
                         const ThinUnit un = sp.units[u];
@@ -143,11 +146,11 @@ thin_layer_kernel(const __nv_bfloat16* __restrict__ x, int k, int H, int I, int 
         } else if (warp - kProducers < nc) {
             constexpr int kExact =
                 (VD > 0 && DownRegSlots<VD>::value > 0) ? DownRegSlots<VD>::value : 16;
-            ok = consume<kExact>(m, rg, ipe, sp.units, warp - kProducers, nc, wait_cycles,
-                                 [&]<int N>(int it, int slot) {
+            ok = consume<kExact, kBufs>(m, rg, ipe, sp.units, warp - kProducers, nc,
+                                        wait_cycles, [&]<int N>(int it, int slot, const Smem& mu) {
                 const ThinUnit un = sp.units[it / ipe];
                 __nv_bfloat16* ycol = y + (int64_t)un.row0 * H + (it % ipe) * Rd;
-                down_slot<N, VD>(m, slot, Rd, vec, un.n, ycol, H);
+                down_slot<N, VD>(mu, slot, Rd, vec, un.n, ycol, H);
             });
         }
         if (!ok) set_status(hdr, MOE_ERR_TIMEOUT);
@@ -155,13 +158,13 @@ thin_layer_kernel(const __nv_bfloat16* __restrict__ x, int k, int H, int I, int 
     combine_spread(sr, sp.inv_perm, sp.gates, hdr, y, H, wait_cycles);
 }
 
-template <int VG, int VD>
+template <int VG, int VD, int kBufs>
 cudaError_t launch_layer(const __nv_bfloat16* x, int k, int H, int I, const __nv_bfloat16* Wg,
                          const __nv_bfloat16* Wu, const __nv_bfloat16* Wd, const Plan& plan,
                          const Geometry& g1, const Geometry& g2, __nv_bfloat16* h,
                          __nv_bfloat16* y, int num_sms, cudaStream_t s, const SelfRoute& sr) {
     static std::atomic<int> done[kMaxDevices];
-    cudaError_t e = smem_limit_once(thin_layer_kernel<VG, VD>, kSmemBudget + 1024, done);
+    cudaError_t e = smem_limit_once(thin_layer_kernel<VG, VD, kBufs>, kSmemBudget + 1024, done);
     if (e != cudaSuccess) return e;
     // every CTA resident at once (the down phase waits for all of them), and
     // allowed to start while the previous kernel on s finishes
@@ -177,7 +180,7 @@ cudaError_t launch_layer(const __nv_bfloat16* x, int k, int H, int I, const __nv
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = t_pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, thin_layer_kernel<VG, VD>, x, k, H, I, g1.R, g2.R, Wg, Wu,
+    return cudaLaunchKernelEx(&cfg, thin_layer_kernel<VG, VD, kBufs>, x, k, H, I, g1.R, g2.R, Wg, Wu,
                               Wd, plan.wslot, plan.hdr, h, y, g1.stage, g1.slots, g1.act,
                               g2.stage, g2.slots, g2.act, sr, main_wait_cycles());
 }
@@ -195,16 +198,20 @@ cudaError_t launch_thin_layer(const __nv_bfloat16* x, int k, int H, int I,
                               cudaStream_t s, const SelfRoute& sr) {
     const int act_tokens =
         (int)std::min<int64_t>(plan.unit_tokens, std::max<int64_t>(max_slots, 1));
-    const Geometry g1 = geometry(2 * H * 2, H * 2, act_tokens, false);
-    const Geometry g2 = geometry(I * 2, I * 2, act_tokens, true);
+    const int bufs = sr.T >= 2 ? 2 : 1;
+    const Geometry g1 = geometry(2 * H * 2, H * 2, act_tokens, false, bufs);
+    const Geometry g2 = geometry(I * 2, I * 2, act_tokens, true, bufs);
     if (g1.stage != kStageTarget || g2.stage != kStageTarget)
         return cudaErrorInvalidConfiguration;
-    if (H == 4096 && I == 2048)
-        return launch_layer<16, 8>(x, k, H, I, Wg, Wu, Wd, plan, g1, g2, h, y_sorted, num_sms, s, sr);
-    if (H == 2048 && I == 1024)
-        return launch_layer<8, 4>(x, k, H, I, Wg, Wu, Wd, plan, g1, g2, h, y_sorted, num_sms, s, sr);
-    if (H == 512 && I == 256)
-        return launch_layer<2, 1>(x, k, H, I, Wg, Wu, Wd, plan, g1, g2, h, y_sorted, num_sms, s, sr);
+#define MOE_LAYER(VG, VD)                                                                     \
+    return bufs == 2 ? launch_layer<VG, VD, 2>(x, k, H, I, Wg, Wu, Wd, plan, g1, g2, h, y_sorted, \
+                                               num_sms, s, sr)                                \
+                     : launch_layer<VG, VD, 1>(x, k, H, I, Wg, Wu, Wd, plan, g1, g2, h, y_sorted, \
+                                               num_sms, s, sr)
+    if (H == 4096 && I == 2048) MOE_LAYER(16, 8);
+    if (H == 2048 && I == 1024) MOE_LAYER(8, 4);
+    if (H == 512 && I == 256) MOE_LAYER(2, 1);
+#undef MOE_LAYER
     return cudaErrorInvalidConfiguration;
 }
 
