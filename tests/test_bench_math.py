@@ -78,3 +78,27 @@ def test_roofline_arithmetic():
     r = bench.roofline_for("combine", work, 2.0, peaks)         # 2 ms: half the peak
     assert r["bound"] == "hbm" and r["unit"] == "GB/s"
     assert r["achieved"] == pytest.approx(3393.6, rel=1e-4) and r["frac"] == pytest.approx(0.5)
+
+
+def test_clock_sampler_window_and_reasons():
+    """The clock summary takes the median SM clock of the samples inside the
+    marked window, the throttle reasons active there, and the whole run's
+    minimum beside them (synthetic nvidia-smi lines; no subprocess)."""
+    clk = bench.ClockSampler(0)
+    line = "{sm}, 2070, 900.5, {hw}, Not Active, Not Active, {pc}"
+    clk.samples = [
+        (0.0, line.format(sm=1500, hw="Not Active", pc="Active")),      # before the window
+        (1.0, line.format(sm=2070, hw="Not Active", pc="Not Active")),
+        (1.1, line.format(sm=2040, hw="Not Active", pc="Active")),
+        (1.2, line.format(sm=2070, hw="Not Active", pc="Not Active")),
+        (3.0, line.format(sm=1200, hw="Active", pc="Not Active")),      # after it
+        (3.1, "garbled"),
+    ]
+    clk.mark(0.9, 1.3)
+    s = clk.summary()
+    assert s["sm_mhz"] == 2070.0 and s["samples"] == 3 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
+    assert s["run"]["sm_mhz_min"] == 1200.0 and s["run"]["samples"] == 5
+    assert s["run"]["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    empty = bench.ClockSampler(0)
+    assert empty.summary()["reasons"] == ["unsampled"]
